@@ -1,0 +1,10 @@
+"""The CPU oracle against the pins (closed forms, invariants, the pages' worked numbers)."""
+
+import pytest
+
+from tests import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin, oracle):
+    pin(oracle)
