@@ -1,0 +1,528 @@
+#!/usr/bin/env python
+"""Benchmark of the AWQ per-linear-layer step on one B300 (or N, one independent layer each).
+
+One step = the whole hot path over one synthetic layer shaped like a Llama-7B attention
+projection (K = N = 4096, T = 8192 calibration tokens, 20 alphas, group 128):
+  calibration statistic -> alpha search (scale grid, per-alpha residual + tcgen05 scoring,
+  argmin) -> final quantise/pack -> W4A16 matmul at M = 1, 4, 16, 128.
+Inputs are resident in HBM when the timed region starts; L2 is flushed (256 MB write) between
+steps, outside the per-step CUDA events. The headline is layers/s; the JSON line also carries the
+roofline of the dominant kernel (the scoring GEMM), per-kernel live timings, an HBM-bound W4A16
+sweep over weight sets larger than L2, the end-to-end number through host buffers, the CPU
+oracle baseline and the SM clocks seen during the timed region.
+
+``--impl reference`` times the CPU oracle instead (bounded samples of the same layer).
+Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under torchrun, every rank
+runs its own layer (weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from post_weight_quantization_stats_b300 import synth  # noqa: E402
+
+METRIC = "W4A16 GEMV/GEMM HBM TB/s & TFLOP/s vs roofline; AWQ search layers/sec"
+UNIT = "layers/s"
+WORKLOAD = "llama7b-attn-4096"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-hbm-sweep", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------ host helpers
+
+def dist_env():
+    """(rank, local_rank, world) from the torchrun environment (defaults: single process)."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def layer_units(wl_name):
+    """Layers one step processes and their shapes (every rank runs one layer of the workload)."""
+    wl = synth.WORKLOADS[wl_name]
+    spec = wl.layers[0]
+    return wl, spec
+
+
+def algorithmic(spec, G, n_alpha, gemm_m):
+    """Algorithmic bytes/flops per launch of each kernel for one layer (N, K, T)."""
+    N, K, T = spec.n, spec.k, spec.t
+    packed = N * K // 2 + 3 * N * (K // G)
+    return {
+        "calib_stats": {"bytes": 2 * T * K + 4 * K},
+        "absmax": {"bytes": 2 * N * K},
+        "residual": {"bytes": 2 * N * K + 8 * K + 2 * N * K},
+        "score": {"flops": 2 * T * N * K},
+        "quantize_pack": {"bytes": 2 * N * K + 4 * K + packed},
+        "gemv": {m: {"bytes": packed + 2 * m * K + 2 * m * N + 4 * K, "flops": 2 * m * N * K}
+                 for m in gemm_m},
+        "packed_bytes": packed,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows):
+    """Median SM clock, max clock and every throttle reason seen Active in the samples."""
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+
+    sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+    mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+    reasons = set()
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    for r in rows:
+        for name, val in zip(names, r[5:9]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def max_over_ranks(value, world):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 0) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_layer_seconds(layer, alphas, gemm_m, G, n_rows, m_cache=None):
+    """Time the oracle on the first ``n_rows`` output rows of the layer (full T and K) and
+    extrapolate linearly in rows to the whole layer. Returns (seconds per layer, detail)."""
+    from oracle import awq_ref as ref
+
+    W, X = layer["W"], layer["X"]
+    N = W.shape[0]
+    t0 = time.perf_counter()
+    m = ref.calib_stats(X) if m_cache is None else m_cache
+    t_stats = time.perf_counter() - t0
+    Ws = W[:n_rows]
+    t1 = time.perf_counter()
+    r = ref.search_scale(Ws, X, alphas, G, m=m)
+    qd = ref.quantize_pack(Ws, r["s"], G)
+    inv = (np.float32(1) / r["s"]).astype(np.float32)
+    for M in gemm_m:
+        ref.w4a16_gemm(X[:M], qd["qweight"], qd["scales"], qd["zeros"], G, inv_s=inv)
+    t_rows = time.perf_counter() - t1
+    stats_time = t_stats if m_cache is None else 0.0
+    per_layer = stats_time + t_rows * (N / n_rows)
+    return per_layer, {"t_stats": t_stats, "t_rows": t_rows, "n_rows": n_rows, "m": m}
+
+
+def choose_rows(layer, alphas, gemm_m, G, budget_s):
+    """Output-row count whose oracle time fits ``budget_s`` (probe with 16 rows, scale)."""
+    N = layer["W"].shape[0]
+    probe = min(16, N)
+    _, d = oracle_layer_seconds(layer, alphas, gemm_m, G, probe)
+    per_row = max(d["t_rows"] / probe, 1e-6)
+    rows = int(max(probe, min(N, budget_s / per_row)))
+    return rows, d["m"]
+
+
+def cpu_baseline(layer, alphas, gemm_m, G, budget_s=12.0):
+    rows, m = choose_rows(layer, alphas, gemm_m, G, budget_s)
+    sec, d = oracle_layer_seconds(layer, alphas, gemm_m, G, rows)
+    N, K = layer["W"].shape
+    T = layer["X"].shape[0]
+    return {"value": 1.0 / sec, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"oracle (fp64 numpy) on {rows} of {N} output rows of the {N}x{K} layer "
+                      f"with all T={T} calibration tokens and {len(alphas)} alphas plus the "
+                      f"M={list(gemm_m)} matmuls; statistic over the full X; time extrapolated "
+                      f"linearly in rows to the whole layer",
+            "seconds_per_layer": sec, "sample_seconds": d["t_stats"] + d["t_rows"]}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    wl, spec = layer_units(args.workload)
+    layer = synth.make_layer(args.workload, 0)
+    alphas = synth.alpha_grid(wl.n_alpha)
+    G = wl.group_size
+    total_steps = args.steps + args.warmup
+    budget = max(1.0, min(8.0, 150.0 / max(total_steps, 1)))
+    rows, m = choose_rows(layer, alphas, wl.gemm_m, G, budget)
+    from oracle import awq_ref as ref
+    t0 = time.perf_counter()
+    ref.calib_stats(layer["X"])                     # the statistic is row-independent: once
+    t_stats = time.perf_counter() - t0
+    per = []
+    for i in range(total_steps):
+        sec, _ = oracle_layer_seconds(layer, alphas, wl.gemm_m, G, rows, m_cache=m)
+        if i >= args.warmup:
+            per.append(sec + t_stats)
+    mean_s = sum(per) / len(per)
+    value = 1.0 / mean_s
+    sample = (f"each step: oracle (fp64 numpy) on {rows} of {spec.n} output rows of the "
+              f"{spec.n}x{spec.k} layer, all T={spec.t} tokens, {len(alphas)} alphas, pack and "
+              f"the M={list(wl.gemm_m)} matmuls, extrapolated linearly in rows; the statistic "
+              f"over the full X is timed once ({t_stats:.2f} s) and added to every step")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "N": spec.n, "K": spec.k, "T": spec.t,
+                   "group_size": G, "n_alpha": len(alphas), "gemm_m": list(wl.gemm_m)},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+class LayerStep:
+    """Device buffers and the enqueue of one full layer step through the C ABI."""
+
+    def __init__(self, awq, torch, layer, wl, dev):
+        self.awq, self.torch = awq, torch
+        W16, X16 = layer["W"], layer["X"]
+        self.N, self.K = W16.shape
+        self.T = X16.shape[0]
+        self.G = wl.group_size
+        self.alphas = synth.alpha_grid(wl.n_alpha)
+        self.gemm_m = tuple(wl.gemm_m)
+        self.W = torch.from_numpy(W16).to(dev)
+        self.X = torch.from_numpy(X16).to(dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.m = torch.empty(self.K, **f32)
+        self.err = torch.empty(len(self.alphas), **f32)
+        self.best = torch.empty(1, dtype=torch.int32, device=dev)
+        self.s = torch.empty(self.K, **f32)
+        self.inv_s = torch.empty(self.K, **f32)
+        self.ws_bytes = awq.awq_search_workspace_bytes(self.N, self.K, self.T, len(self.alphas),
+                                                       self.G)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.q = torch.empty((self.N, self.K // 8), dtype=torch.int32, device=dev)
+        self.sc = torch.empty((self.K // self.G, self.N), dtype=torch.float16, device=dev)
+        self.z = torch.empty((self.K // self.G, self.N), dtype=torch.uint8, device=dev)
+        self.ym = {M: torch.empty((M, self.N), dtype=torch.float16, device=dev)
+                   for M in self.gemm_m}
+        self.stream = torch.cuda.current_stream()
+
+    def enqueue(self):
+        a, st = self.awq, self.stream
+        a.awq_calib_stats(self.X, self.T, self.K, self.K, self.m, st)
+        a.awq_search_scale(self.W, self.N, self.K, self.X, self.T, self.m, self.alphas,
+                           len(self.alphas), self.G, False, self.ws, self.ws_bytes, self.err,
+                           self.best, self.s, self.inv_s, st)
+        a.awq_quantize_pack(self.W, self.N, self.K, self.s, self.G, False, self.q, self.sc,
+                            self.z, st)
+        for M in self.gemm_m:
+            # the first M calibration rows serve as the batch (a contiguous prefix of X)
+            a.awq_w4a16_gemm(self.X, M, self.N, self.K, self.q, self.sc, self.z, self.inv_s,
+                             self.G, False, self.ym[M], st)
+
+    def outputs(self):
+        return [self.err, self.best, self.s, self.inv_s, self.q, self.sc, self.z] + \
+            [self.ym[M] for M in self.gemm_m]
+
+
+def hbm_sweep(awq, torch, N, K, G, ms, peaks, reps=20):
+    """W4A16 at each M over weight sets whose total exceeds 2x L2, so every launch streams its
+    weights from HBM. Per-launch time from the library's event pairs."""
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size if hasattr(
+        torch.cuda.get_device_properties(0), "L2_cache_size") else 126 * 2 ** 20
+    packed = N * K // 2 + 3 * N * (K // G)
+    copies = int(max(2, -(-2 * l2 // packed)))
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    sets = []
+    for _ in range(copies):
+        q = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32, device="cuda",
+                          generator=gen)
+        sc = (torch.rand((K // G, N), device="cuda", generator=gen) * 0.01 + 1e-3).half()
+        z = torch.randint(0, 16, (K // G, N), dtype=torch.uint8, device="cuda", generator=gen)
+        sets.append((q, sc, z))
+    out = []
+    for M in ms:
+        X = (torch.randn((M, K), device="cuda", generator=gen)).half()
+        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        for i in range(copies):  # warm-up (code paths, TMA descriptors)
+            q, sc, z = sets[i]
+            awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, None, G, False, Y)
+        torch.cuda.synchronize()
+        awq.awq_profile_begin()
+        for r in range(reps):
+            for i in range(copies):
+                q, sc, z = sets[i]
+                awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, None, G, False, Y)
+        prof = awq.awq_profile_end()
+        name = "gemv" if M <= 8 else "gemm_tc"
+        n, ms_tot = prof[name]
+        us = ms_tot * 1e3 / n
+        byts = packed + 2 * M * K + 2 * M * N
+        gbs = byts / (us * 1e-6) / 1e9
+        tfl = 2 * M * N * K / (us * 1e-6) / 1e12
+        out.append({"M": M, "N": N, "K": K, "kernel": name, "us": round(us, 3),
+                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                    "TFLOP/s": round(tfl, 2), "frac_tensor": round(tfl / peaks["bf16_tflops"], 4),
+                    "weight_sets": copies})
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+
+    from post_weight_quantization_stats_b300 import awq
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    awq.lib()
+    peaks = measured_peaks()
+    wl, spec = layer_units(args.workload)
+    layer = synth.make_layer(args.workload, rank % len(wl.layers) if len(wl.layers) > 1 else 0)
+    if rank > 0 and len(wl.layers) == 1:  # an independent layer per rank (own seed)
+        layer = synth.make_layer(synth.Workload(wl.wid * 100 + rank, wl.name, wl.layers,
+                                                wl.gemm_m), 0)
+    dev = torch.device("cuda", local_rank)
+    step = LayerStep(awq, torch, layer, wl, dev)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(args.warmup, 0)):
+        step.enqueue()
+    awq.awq_stream_status()
+
+    props = torch.cuda.get_device_properties(local_rank)
+    bus = None
+    if hasattr(props, "pci_bus_id"):
+        bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:" \
+              f"{getattr(props, 'pci_device_id', 0):02X}.0"
+    clocks = ClockSampler(bus).start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = awq.awq_launch_count()
+    awq.awq_profile_begin()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record()
+        step.enqueue()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    prof = awq.awq_profile_end()
+    barrier(world)
+    launches = awq.awq_launch_count() - launches0
+    clk = clocks.stop()
+    awq.awq_stream_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+
+    alg = algorithmic(spec, step.G, len(step.alphas), step.gemm_m)
+    kern = {}
+    for name, (n, ms_tot) in prof.items():
+        avg_us = ms_tot * 1e3 / n
+        row = {"launches": n, "avg_us": round(avg_us, 3), "share": None}
+        if name in alg and "bytes" in alg[name]:
+            row["GB/s"] = round(alg[name]["bytes"] / (avg_us * 1e-6) / 1e9, 1)
+        if name == "score":
+            row["TFLOP/s"] = round(alg["score"]["flops"] / (avg_us * 1e-6) / 1e12, 1)
+        kern[name] = row
+    tot_kernel_ms = sum(ms for _, ms in prof.values())
+    for name, (n, ms_tot) in prof.items():
+        kern[name]["share"] = round(ms_tot / tot_kernel_ms, 4) if tot_kernel_ms else None
+    n_score, ms_score = prof.get("score", (0, 0.0))
+    score_avg_s = ms_score / 1e3 / max(n_score, 1)
+    achieved = alg["score"]["flops"] / score_avg_s / 1e12 if n_score else None
+    roofline = {"bound": "tensor", "kernel": "score_kernel (tcgen05 kind::f16, fp32 accumulate)",
+                "achieved": round(achieved, 1) if achieved else None,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4) if achieved else None,
+                "traffic": None,
+                "peak_note": f"{peaks['source']} dense bf16 burst (fp16 runs at the bf16 rate); "
+                             f"sustained {peaks['bf16_tflops_sustained']}",
+                "flops_per_launch": alg["score"]["flops"]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": args.workload, "N": step.N, "K": step.K, "T": step.T,
+                   "group_size": step.G, "n_alpha": len(step.alphas),
+                   "gemm_m": list(step.gemm_m), "l2": "flushed between steps (256 MB write)",
+                   "parallelism": f"replicas x{world}: one independent layer per GPU"},
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "kernels": kern,
+        "clocks": clk,
+        "wall_s_timed": round(t_wall, 4),
+    }
+    if rank == 0 and not args.no_hbm_sweep:
+        line["w4a16_hbm"] = hbm_sweep(awq, torch, step.N, step.K, step.G, step.gemm_m, peaks)
+        g1 = [r for r in line["w4a16_hbm"] if r["M"] == 1]
+        if g1:
+            line["roofline_gemv_m1"] = {"bound": "hbm", "achieved": g1[0]["GB/s"],
+                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": g1[0]["frac_hbm"], "traffic": None}
+    if not args.no_e2e:
+        line["e2e"] = e2e_run(awq, torch, step, layer, args, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(layer, step.alphas, step.gemm_m, step.G)
+        line["cpu_baseline"].pop("seconds_per_layer", None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_run(awq, torch, step, layer, args, world):
+    """The same step through the public API from pinned host buffers: H2D of W and X, the step,
+    D2H of every result, all inside the timed region."""
+    W_h = torch.from_numpy(layer["W"]).pin_memory()
+    X_h = torch.from_numpy(layer["X"]).pin_memory()
+    outs = step.outputs()
+    hosts = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = W_h.numel() * 2 + X_h.numel() * 2
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def one():
+        step.W.copy_(W_h, non_blocking=True)
+        step.X.copy_(X_h, non_blocking=True)
+        step.enqueue()
+        for h, o in zip(hosts, outs):
+            h.copy_(o, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = max_over_ranks(time.perf_counter() - t0, world)
+    return {"value": world * args.steps / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+/*
+ * awq.h - C ABI of libawq: the AWQ per-linear-layer step and the W4A16 matmul on one GPU
+ * (B300, sm_103a).
+ *
+ * What the calls compute, with the passages they follow (page title, section):
+ *
+ *   awq_calib_stats    m_j = mean over calibration tokens of |x_j|
+ *                      ("AWQ Math", "Saliency is an activation property, not a weight property")
+ *   awq_search_scale   s = max(m, 1e-6)^alpha for each alpha of a grid; W' = W diag(s) quantised
+ *                      group-wise to 4 bits; E(alpha) = mean over tokens and outputs of
+ *                      (W x - Q(W') diag(s)^-1 x)^2; alpha* = the first minimiser
+ *                      ("AWQ Math", "The equivalent transform", "Searching the scale")
+ *   awq_quantize_pack  4-bit codes of W diag(s), one step and one zero point per group of
+ *                      input channels ("AWQ Math", "Weight-only quantization and where it
+ *                      breaks" and "Shapes, granularity, and complexity")
+ *   awq_w4a16_gemm     Y = X (dequant(Q) diag(inv_s))^T without materialising fp16 weights
+ *                      ("AWQ > Benefits and Practical Considerations": unpack the 4-bit
+ *                      integers, apply the group scale and zero point and, optionally, the
+ *                      per-channel inverse scale, fused with the matmul)
+ *
+ * Quantiser (fp32, IEEE rounding, no FMA contraction; rint = round half to even):
+ *   asymmetric: hi = max(max w', 0), lo = min(min w', 0), step = (hi - lo) / 15 (1 if 0),
+ *               z = clamp(rint(-lo / step), 0, 15), q = clamp(rint(w' / step) + z, 0, 15)
+ *   symmetric:  step = max|w'| / 8 (1 if 0), q = clamp(rint(w' / step), -8, 7) + 8, z = 8
+ *   w' = fp32(W * s). Stored step = fp16 (round to nearest even) of the fp32 step.
+ *
+ * Packed format (the one every call reads and writes):
+ *   qweight [N, K/8] uint32, row-major: nibble i (bits 4i..4i+3) of qweight[n][w] is the
+ *           code of input channel k = 8w + i.
+ *   scales  [K/G, N] fp16: step of group g (channels gG .. gG+G-1) of output row n at g*N + n.
+ *   zeros   [K/G, N] uint8: zero point, same indexing; not read or written in symmetric mode
+ *           (the zero point is 8 there).
+ *
+ * Conventions for every call:
+ *   - Pointers are device pointers owned by the caller, except `alphas`, a host array. Every
+ *     device pointer must be 16-byte aligned. The library allocates no device memory; scratch
+ *     for the search comes from the caller's workspace.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and is
+ *     asynchronous: results are valid once the stream has been synchronised.
+ *   - Arguments are checked on the host before anything is enqueued; a failed check returns
+ *     an error code and enqueues nothing. Kernel launch failures return AWQ_ERR_CUDA.
+ *   - The pipelined tensor-core kernels bound every wait; a kernel that gives up records
+ *     AWQ_ERR_TIMEOUT in a device status word that awq_stream_status reports.
+ *   - Shapes: G (group size) is 64 or 128, K % G == 0, all sizes >= 1, and N * K, T * K and
+ *     M * max(N, K) below 2^31 elements.
+ */
+#ifndef AWQ_H_
+#define AWQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* awq_stream_t; /* same object as cudaStream_t */
+
+typedef enum {
+  AWQ_OK = 0,
+  AWQ_ERR_INVALID_ARG = 1,       /* NULL pointer, non-positive size, bad group size/alpha count */
+  AWQ_ERR_UNSUPPORTED_SHAPE = 2, /* K % G != 0, ldx < K or not a multiple of 8, size limits */
+  AWQ_ERR_MISALIGNED = 3,        /* a device pointer is not 16-byte aligned */
+  AWQ_ERR_WORKSPACE = 4,         /* workspace NULL or smaller than awq_search_workspace_bytes */
+  AWQ_ERR_CUDA = 5,              /* a CUDA runtime/driver call or kernel launch failed */
+  AWQ_ERR_TIMEOUT = 6,           /* a device-side bounded wait gave up (see awq_stream_status) */
+  AWQ_ERR_NO_DEVICE = 7          /* no usable device, or the device is not sm_103 */
+} awq_status_t;
+
+typedef struct {
+  int32_t group_size; /* 64 or 128 input channels per (step, zero point) */
+  int32_t symmetric;  /* 0: asymmetric with zero point; 1: step = max|w| / 8, zero point 8 */
+} awq_qcfg_t;
+
+/*
+ * Per-input-channel calibration statistic.
+ *   X_f16    [T, ldx] fp16 row-major, the first K columns are used (calibration activations)
+ *   mean_abs [K] fp32 out: (1/T) sum_t |X[t, j]| (fp32 accumulation, deterministic order)
+ * Requires ldx >= K and ldx % 8 == 0, K % 8 == 0.
+ */
+awq_status_t awq_calib_stats(const void* X_f16, int64_t T, int64_t K, int64_t ldx,
+                             float* mean_abs, awq_stream_t stream);
+
+/* Bytes of device workspace awq_search_scale needs for this shape (0 on invalid input). */
+size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
+                                  awq_qcfg_t cfg);
+
+/*
+ * The alpha search of one linear layer.
+ *   W_f16    [N, K] fp16 row-major: the layer weight W [C_out, C_in]
+ *   X_f16    [T, K] fp16 row-major: calibration activations
+ *   mean_abs [K] fp32 statistic from awq_calib_stats, or NULL to compute it here
+ *   alphas   host [n_alpha] fp32 exponents (1 <= n_alpha <= 64), e.g. i/20 for i < 20
+ *   workspace / ws_bytes   device scratch of at least awq_search_workspace_bytes(...)
+ *   err_out  [n_alpha] fp32 out: E(alpha_i)
+ *   best_idx [1] int32 out: first i with the smallest E (computed in fp64)
+ *   s_out    [K] fp32 out (may be NULL): s = max(m, 1e-6)^alpha* as used for the codes
+ *   inv_s_out[K] fp32 out (may be NULL): 1 / s (IEEE division), the GEMM's inv_s
+ * The scales are computed in fp64 and rounded to fp32; the codes behind E(alpha_i) are exactly
+ * those awq_quantize_pack produces for s_i.
+ */
+awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
+                              int64_t T, const float* mean_abs, const float* alphas,
+                              int32_t n_alpha, awq_qcfg_t cfg, void* workspace,
+                              size_t ws_bytes, float* err_out, int32_t* best_idx,
+                              float* s_out, float* inv_s_out, awq_stream_t stream);
+
+/*
+ * Group-wise 4-bit quantisation of W diag(s) into the packed format above.
+ *   W_f16   [N, K] fp16;  s [K] fp32 per-input-channel scale, or NULL for s = 1 (plain RTN)
+ *   qweight [N, K/8] uint32 out; scales_f16 [K/G, N] fp16 out; zeros [K/G, N] uint8 out
+ *   (zeros may be NULL in symmetric mode).
+ */
+awq_status_t awq_quantize_pack(const void* W_f16, int64_t N, int64_t K, const float* s,
+                               awq_qcfg_t cfg, uint32_t* qweight, void* scales_f16,
+                               uint8_t* zeros, awq_stream_t stream);
+
+/*
+ * W4A16 dequant-fused matmul: Y [M, N] fp16 = X [M, K] fp16 @ (dequant(Q) diag(inv_s))^T,
+ * fp32 accumulation. inv_s [K] fp32 or NULL (1/s already folded into the previous layer).
+ * M <= 8 runs a CUDA-core GEMV; larger M runs the tcgen05 tensor-core kernel. With inv_s,
+ * X * inv_s must stay inside the fp16 range (as the folded activation would).
+ */
+awq_status_t awq_w4a16_gemm(const void* X_f16, int64_t M, int64_t N, int64_t K,
+                            const uint32_t* qweight, const void* scales_f16,
+                            const uint8_t* zeros, const float* inv_s, awq_qcfg_t cfg,
+                            void* Y_f16, awq_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* awq_status_string(awq_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the current device:
+ * AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the last call, AWQ_ERR_CUDA if the
+ * synchronisation failed, else AWQ_OK.
+ */
+awq_status_t awq_stream_status(awq_stream_t stream);
+
+/* Number of kernels this library has launched in this process (diagnostic counter). */
+uint64_t awq_launch_count(void);
+
+/*
+ * Limit, in nanoseconds, of every bounded device-side wait in later launches (default 2e9).
+ * Returns the previous value.
+ */
+uint64_t awq_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Kernels of this library, as counted by the profiling calls below. */
+typedef enum {
+  AWQ_K_CALIB_STATS = 0, /* awq_calib_stats (and the search when mean_abs is NULL) */
+  AWQ_K_SCALE_GRID = 1,  /* search: s and 1/s for every alpha */
+  AWQ_K_ABSMAX = 2,      /* search: max|W| for the residual's power-of-two scale */
+  AWQ_K_RESIDUAL = 3,    /* search: W - Q(W diag s) diag(s)^-1 of one alpha, fp16 */
+  AWQ_K_SCORE = 4,       /* search: tcgen05 sum of squares of X D^T of one alpha */
+  AWQ_K_FINALIZE = 5,    /* search: errors, argmin, winning scales */
+  AWQ_K_QUANTIZE_PACK = 6,
+  AWQ_K_GEMV = 7,        /* awq_w4a16_gemm, M <= 8 */
+  AWQ_K_GEMM_TC = 8,     /* awq_w4a16_gemm, M > 8 */
+  AWQ_K_COUNT = 9
+} awq_kernel_id_t;
+
+/*
+ * Profiling aid. After awq_profile_begin, every launch of this library (any thread, any
+ * stream) is bracketed by a CUDA event pair recorded on its own stream. awq_profile_end
+ * synchronises those events, stops recording and writes, per awq_kernel_id_t, the summed
+ * kernel time in ms (total_ms[AWQ_K_COUNT]) and the launch count (launches[AWQ_K_COUNT]);
+ * either output may be NULL. Events are created on first use and reused.
+ */
+awq_status_t awq_profile_begin(void);
+awq_status_t awq_profile_end(double* total_ms, uint64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AWQ_H_ */

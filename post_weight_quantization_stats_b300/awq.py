@@ -1,0 +1,228 @@
+"""Thin Python binding of libawq (``include/awq.h``): argument marshalling only.
+
+The ``awq_*`` functions mirror the C entry points one to one; pointer arguments accept an
+integer address or a CUDA ``torch.Tensor`` (its ``data_ptr()``), ``stream`` accepts a
+``torch.cuda.Stream``, a raw handle or ``None`` (torch's current stream). A non-zero status
+raises :class:`AwqError`. The convenience wrappers at the bottom only allocate outputs with
+torch and call the same entry points; every step of the computation runs in the library's CUDA
+kernels. There is no fallback: without the built library or a B300 the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libawq.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "awq.h")
+
+STATUS = {
+    0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_UNSUPPORTED_SHAPE",
+    3: "AWQ_ERR_MISALIGNED", 4: "AWQ_ERR_WORKSPACE", 5: "AWQ_ERR_CUDA", 6: "AWQ_ERR_TIMEOUT",
+    7: "AWQ_ERR_NO_DEVICE",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+
+class AwqError(RuntimeError):
+    """A libawq call returned a non-zero awq_status_t."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = int(status)
+        self.name = STATUS.get(int(status), f"status {status}")
+        super().__init__(f"{fn}: {self.name}")
+
+
+class QCfg(ctypes.Structure):
+    _fields_ = [("group_size", ctypes.c_int32), ("symmetric", ctypes.c_int32)]
+
+
+_c_void_p, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+
+_SIGNATURES = {
+    "awq_calib_stats": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p]),
+    "awq_search_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, QCfg]),
+    "awq_search_scale": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i64, _c_void_p,
+                                        _c_void_p, _i32, QCfg, _c_void_p, _sz, _c_void_p,
+                                        _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "awq_quantize_pack": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, QCfg, _c_void_p,
+                                         _c_void_p, _c_void_p, _c_void_p]),
+    "awq_w4a16_gemm": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
+                                      _c_void_p, _c_void_p, QCfg, _c_void_p, _c_void_p]),
+    "awq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "awq_stream_status": (ctypes.c_int, [_c_void_p]),
+    "awq_launch_count": (ctypes.c_uint64, []),
+    "awq_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "awq_profile_begin": (ctypes.c_int, []),
+    "awq_profile_end": (ctypes.c_int, [_c_void_p, _c_void_p]),
+}
+
+KERNELS = ("calib_stats", "scale_grid", "absmax", "residual", "score", "finalize",
+           "quantize_pack", "gemv", "gemm_tc")
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libawq.so from the package directory (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m post_weight_quantization_stats_b300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def header_functions() -> list:
+    """Names of every function the C header declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(awq_[a-z0-9_]+)\s*\(", text)))
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _cfg(group_size=128, symmetric=False) -> QCfg:
+    return QCfg(int(group_size), 1 if symmetric else 0)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise AwqError(fn, status)
+
+
+# ----------------------------------------------------------------------------- C entry points
+
+def awq_calib_stats(X, T, K, ldx, mean_abs, stream=None):
+    _check("awq_calib_stats", lib().awq_calib_stats(_ptr(X), T, K, ldx, _ptr(mean_abs),
+                                                    _stream(stream)))
+
+
+def awq_search_workspace_bytes(N, K, T, n_alpha, group_size=128, symmetric=False) -> int:
+    return int(lib().awq_search_workspace_bytes(N, K, T, n_alpha, _cfg(group_size, symmetric)))
+
+
+def awq_search_scale(W, N, K, X, T, mean_abs, alphas, n_alpha, group_size, symmetric, workspace,
+                     ws_bytes, err_out, best_idx, s_out, inv_s_out, stream=None):
+    arr = (ctypes.c_float * int(n_alpha))(*[float(a) for a in alphas])
+    _check("awq_search_scale", lib().awq_search_scale(
+        _ptr(W), N, K, _ptr(X), T, _ptr(mean_abs), ctypes.cast(arr, ctypes.c_void_p), n_alpha,
+        _cfg(group_size, symmetric), _ptr(workspace), ws_bytes, _ptr(err_out), _ptr(best_idx),
+        _ptr(s_out), _ptr(inv_s_out), _stream(stream)))
+
+
+def awq_quantize_pack(W, N, K, s, group_size, symmetric, qweight, scales, zeros, stream=None):
+    _check("awq_quantize_pack", lib().awq_quantize_pack(
+        _ptr(W), N, K, _ptr(s), _cfg(group_size, symmetric), _ptr(qweight), _ptr(scales),
+        _ptr(zeros), _stream(stream)))
+
+
+def awq_w4a16_gemm(X, M, N, K, qweight, scales, zeros, inv_s, group_size, symmetric, Y,
+                   stream=None):
+    _check("awq_w4a16_gemm", lib().awq_w4a16_gemm(
+        _ptr(X), M, N, K, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s),
+        _cfg(group_size, symmetric), _ptr(Y), _stream(stream)))
+
+
+def awq_status_string(status: int) -> str:
+    return lib().awq_status_string(int(status)).decode()
+
+
+def awq_stream_status(stream=None):
+    _check("awq_stream_status", lib().awq_stream_status(_stream(stream)))
+
+
+def awq_launch_count() -> int:
+    return int(lib().awq_launch_count())
+
+
+def awq_set_wait_limit_ns(limit_ns: int) -> int:
+    return int(lib().awq_set_wait_limit_ns(int(limit_ns)))
+
+
+def awq_profile_begin():
+    _check("awq_profile_begin", lib().awq_profile_begin())
+
+
+def awq_profile_end() -> dict:
+    """{kernel name: (launches, total ms)} of the launches since awq_profile_begin."""
+    n = len(KERNELS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_uint64 * n)()
+    _check("awq_profile_end", lib().awq_profile_end(ctypes.cast(ms, ctypes.c_void_p),
+                                                    ctypes.cast(cnt, ctypes.c_void_p)))
+    return {k: (int(cnt[i]), float(ms[i])) for i, k in enumerate(KERNELS) if cnt[i]}
+
+
+# ----------------------------------------------------------------------------- tensor helpers
+
+def calib_stats(X, stream=None):
+    """m [K] fp32 = mean |X| over rows of a CUDA fp16 [T, K] tensor."""
+    import torch
+    T, K = X.shape
+    m = torch.empty(K, dtype=torch.float32, device=X.device)
+    awq_calib_stats(X, T, K, X.stride(0), m, stream)
+    return m
+
+
+def quantize_pack(W, s=None, group_size=128, symmetric=False, stream=None):
+    """(qweight [N, K/8] int32, scales [K/G, N] fp16, zeros [K/G, N] uint8) of W diag(s)."""
+    import torch
+    N, K = W.shape
+    q = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    sc = torch.empty((K // group_size, N), dtype=torch.float16, device=W.device)
+    z = torch.empty((K // group_size, N), dtype=torch.uint8, device=W.device)
+    awq_quantize_pack(W, N, K, s, group_size, symmetric, q, sc, z, stream)
+    return q, sc, z
+
+
+def search_scale(W, X, alphas, group_size=128, symmetric=False, mean_abs=None, workspace=None,
+                 stream=None):
+    """The alpha search: returns (err [n] fp32, best_idx [1] int32, s [K], inv_s [K])."""
+    import torch
+    N, K = W.shape
+    T = X.shape[0]
+    n = len(alphas)
+    ws_bytes = awq_search_workspace_bytes(N, K, T, n, group_size, symmetric)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=W.device)
+    err = torch.empty(n, dtype=torch.float32, device=W.device)
+    best = torch.empty(1, dtype=torch.int32, device=W.device)
+    s = torch.empty(K, dtype=torch.float32, device=W.device)
+    inv_s = torch.empty(K, dtype=torch.float32, device=W.device)
+    awq_search_scale(W, N, K, X, T, mean_abs, alphas, n, group_size, symmetric, workspace,
+                     workspace.numel(), err, best, s, inv_s, stream)
+    return err, best, s, inv_s
+
+
+def w4a16_gemm(X, qweight, scales, zeros, inv_s=None, group_size=128, symmetric=False,
+               stream=None):
+    """Y [M, N] fp16 = X [M, K] (dequant(Q) diag(inv_s))^T."""
+    import torch
+    M, K = X.shape
+    N = qweight.shape[0]
+    Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    awq_w4a16_gemm(X, M, N, K, qweight, scales, zeros, inv_s, group_size, symmetric, Y, stream)
+    return Y

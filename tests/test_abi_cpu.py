@@ -1,0 +1,97 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function the header
+declares, and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+import subprocess
+
+import pytest
+
+from post_weight_quantization_stats_b300 import awq, build
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return awq.lib()
+
+
+def test_header_declares_the_boundary():
+    names = awq.header_functions()
+    for fn in ("awq_calib_stats", "awq_search_scale", "awq_quantize_pack", "awq_w4a16_gemm",
+               "awq_search_workspace_bytes", "awq_status_string", "awq_stream_status"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", awq.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for fn in awq.header_functions():
+        assert fn in exported, fn
+        assert hasattr(L, fn)
+
+
+def test_status_strings(L):
+    for code, name in awq.STATUS.items():
+        assert awq.awq_status_string(code) == name
+
+
+def test_workspace_bytes(L):
+    n = awq.awq_search_workspace_bytes(4096, 4096, 8192, 20)
+    assert n >= 4096 * 4096 * 2          # the fp16 residual of one candidate
+    assert n < 4096 * 4096 * 2 + (4 << 20)
+    assert awq.awq_search_workspace_bytes(4096, 4100, 8192, 20) == 0   # K % G
+    assert awq.awq_search_workspace_bytes(4096, 4096, 8192, 65) == 0   # too many alphas
+    assert awq.awq_search_workspace_bytes(4096, 4096, 8192, 20, group_size=96) == 0
+
+
+def _code(L, fn, *args):
+    return getattr(L, fn)(*args)
+
+
+def test_host_validation_rejects_without_cuda(L):
+    cfg = awq.QCfg(128, 0)
+    A = 1 << 20   # a fake, 16-byte aligned address: never dereferenced (rejected first)
+    S = awq.STATUS_CODE
+    # NULL pointers / sizes
+    assert _code(L, "awq_calib_stats", None, 8, 128, 128, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert _code(L, "awq_calib_stats", A, 0, 128, 128, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert _code(L, "awq_calib_stats", A, 8, 128, 100, A, None) == S["AWQ_ERR_UNSUPPORTED_SHAPE"]
+    assert _code(L, "awq_calib_stats", A + 2, 8, 128, 128, A, None) == S["AWQ_ERR_MISALIGNED"]
+    assert _code(L, "awq_quantize_pack", A, 16, 100, None, cfg, A, A, A, None) == \
+        S["AWQ_ERR_UNSUPPORTED_SHAPE"]
+    assert _code(L, "awq_quantize_pack", A, 16, 256, None, awq.QCfg(32, 0), A, A, A, None) == \
+        S["AWQ_ERR_INVALID_ARG"]
+    assert _code(L, "awq_quantize_pack", A, 16, 256, None, cfg, A, A, None, None) == \
+        S["AWQ_ERR_INVALID_ARG"]                          # asymmetric needs zeros
+    assert _code(L, "awq_quantize_pack", A, 16, 256, A + 4, cfg, A, A, A, None) == \
+        S["AWQ_ERR_MISALIGNED"]
+    assert _code(L, "awq_w4a16_gemm", A, 0, 16, 256, A, A, A, None, cfg, A, None) == \
+        S["AWQ_ERR_INVALID_ARG"]
+    assert _code(L, "awq_w4a16_gemm", A, 4, 16, 256, A, A, A, None, cfg, A + 8, None) == \
+        S["AWQ_ERR_MISALIGNED"]
+    alphas = (ctypes.c_float * 2)(0.0, 0.5)
+    ap = ctypes.cast(alphas, ctypes.c_void_p)
+    ws = awq.awq_search_workspace_bytes(16, 256, 8, 2)
+    assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, ap, 2, cfg, A, ws - 1, A, A,
+                 None, None, None) == S["AWQ_ERR_WORKSPACE"]
+    assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, ap, 0, cfg, A, ws, A, A,
+                 None, None, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, None, 2, cfg, A, ws, A, A,
+                 None, None, None) == S["AWQ_ERR_INVALID_ARG"]
+
+
+def test_valid_call_without_a_gpu_reports_no_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    cfg = awq.QCfg(128, 0)
+    A = 1 << 20
+    assert _code(L, "awq_quantize_pack", A, 16, 256, None, cfg, A, A, A, None) == \
+        awq.STATUS_CODE["AWQ_ERR_NO_DEVICE"]
+
+
+def test_launch_counter_starts_without_launches(L):
+    assert awq.awq_launch_count() >= 0
+    old = awq.awq_set_wait_limit_ns(123)
+    assert awq.awq_set_wait_limit_ns(old) == 123

@@ -1,0 +1,271 @@
+"""GPU parity: every CUDA entry point against the CPU oracle on the same seeded inputs.
+
+Bars: packed codes, scales and zero points bit-exact (the oracle is fed the GPU's fp32 scale
+vector, so both sides decide each code in fp32 from the same operands); the statistic within
+1e-5 relative (fp32 accumulation vs fp64); the alpha errors within 1e-3 relative and the chosen
+alpha index exact (unless the oracle's own errors are a near-tie within 1e-4); W4A16 outputs
+within 2e-2 of max|reference| against the oracle's fp64 dequant-matmul.
+"""
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+from oracle import awq_ref as ref  # noqa: E402
+from post_weight_quantization_stats_b300 import awq, build, synth  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    awq.lib()
+    torch.cuda.set_device(0)
+    yield
+    awq.awq_stream_status()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def layer(seed, n, k, t, n_out=0, mult=20.0, student=False):
+    return synth.random_layer(seed, n, k, t, n_out=n_out, mult=mult, student_t=student)
+
+
+# ----------------------------------------------------------------------------- statistic
+
+@pytest.mark.parametrize("T,K,ldx", [(64, 512, 512), (1, 8, 8), (1000, 200, 200),
+                                     (333, 4096, 4104), (8192, 4096, 4096), (129, 11008, 11008)])
+def test_calib_stats(T, K, ldx):
+    rng = np.random.Generator(np.random.PCG64(T * 7 + K))
+    Xfull = (rng.standard_normal((T, ldx)) * 3).astype(np.float16)
+    m = torch.empty(K, dtype=torch.float32, device="cuda")
+    Xd = dev(Xfull)
+    awq.awq_calib_stats(Xd, T, K, ldx, m)
+    awq.awq_stream_status()
+    want = ref.calib_stats(Xfull[:, :K])
+    np.testing.assert_allclose(host(m), want, rtol=1e-5, atol=0)
+
+
+def test_calib_stats_deterministic():
+    X = dev((np.random.Generator(np.random.PCG64(1)).standard_normal((4096, 4096))).astype(np.float16))
+    a, b = awq.calib_stats(X), awq.calib_stats(X)
+    assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------------------- quantize + pack
+
+QP_SHAPES = [(512, 512), (300, 1152), (1, 128), (7, 64), (33, 4096)]
+
+
+@pytest.mark.parametrize("N,K", QP_SHAPES)
+@pytest.mark.parametrize("G", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("with_s", [False, True])
+def test_quantize_pack_bitexact(N, K, G, sym, with_s):
+    if K % G:
+        pytest.skip("K % G")
+    d = layer(N * 31 + K + G, N, K, 4)
+    W16 = d["W"]
+    rng = np.random.Generator(np.random.PCG64(N + K))
+    s = np.exp(rng.uniform(-2, 3, K)).astype(np.float32) if with_s else None
+    q, sc, z = awq.quantize_pack(dev(W16), dev(s) if with_s else None, G, sym)
+    awq.awq_stream_status()
+    want = ref.quantize_pack(W16, s, G, sym)
+    assert np.array_equal(host(q).view(np.uint32), want["qweight"])
+    assert np.array_equal(host(sc), want["scales"])
+    if not sym:
+        assert np.array_equal(host(z), want["zeros"])
+
+
+def test_quantize_pack_special_groups():
+    """All-zero, all-positive, all-negative and constant groups, and exact half-way codes."""
+    K = 256
+    W = np.zeros((6, K), np.float16)
+    W[1] = 0.5
+    W[2, :128] = -np.linspace(0.01, 1, 128)
+    W[2, 128:] = np.linspace(0.01, 1, 128)
+    W[3] = (np.arange(K) % 31 - 15) * 2.0 ** -5            # ladder with half-way points
+    W[4] = (np.arange(K) % 16) * 2.0 ** -6
+    W[5, ::2] = 65504.0 / 4
+    W = W.astype(np.float16)
+    for sym in (False, True):
+        for G in (64, 128):
+            q, sc, z = awq.quantize_pack(dev(W), None, G, sym)
+            want = ref.quantize_pack(W, None, G, sym)
+            assert np.array_equal(host(q).view(np.uint32), want["qweight"])
+            assert np.array_equal(host(sc), want["scales"])
+            if not sym:
+                assert np.array_equal(host(z), want["zeros"])
+
+
+def test_quantize_pack_full_size_sampled_rows():
+    """Llama-70B up-projection shape 28672 x 8192: every code of 64 sampled rows."""
+    d = synth.make_layer("llama70b-mlp", 0, t=8)
+    W16 = d["W"]
+    N, K = W16.shape
+    rng = np.random.Generator(np.random.PCG64(5))
+    s = np.exp(rng.uniform(-1, 2, K)).astype(np.float32)
+    q, sc, z = awq.quantize_pack(dev(W16), dev(s))
+    awq.awq_stream_status()
+    rows = np.sort(rng.choice(N, 64, replace=False))
+    want = ref.quantize_pack(W16[rows], s)
+    assert np.array_equal(host(q)[rows].view(np.uint32), want["qweight"])
+    assert np.array_equal(host(sc)[:, rows], want["scales"])
+    assert np.array_equal(host(z)[:, rows], want["zeros"])
+
+
+# ----------------------------------------------------------------------------- search
+
+def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False):
+    W, X = dev(W16), dev(X16)
+    m = awq.calib_stats(X) if use_m else None
+    err, best, s, inv_s = awq.search_scale(W, X, alphas, G, sym, mean_abs=m)
+    awq.awq_stream_status()
+    m_gpu = host(awq.calib_stats(X))
+    r = ref.search_scale(W16, X16, alphas, G, sym, m=m_gpu)
+    e = host(err).astype(np.float64)
+    np.testing.assert_allclose(e, r["err"], rtol=1e-3, atol=0)
+    b = int(host(best)[0])
+    if b != r["best"]:
+        assert r["err"][b] <= r["err"][r["best"]] * (1 + 1e-4), (b, r["best"], r["err"])
+    np.testing.assert_array_equal(host(s), r["s_grid"][b])
+    np.testing.assert_array_equal(host(inv_s), (np.float32(1) / r["s_grid"][b]).astype(np.float32))
+    return e, b, r
+
+
+def test_search_tiny_layer():
+    d = synth.make_layer("tiny-512")
+    e, b, r = _check_search(d["W"], d["X"], synth.alpha_grid(20))
+    assert b == r["best"] and b > 0
+    assert e[b] <= e[0]
+
+
+@pytest.mark.parametrize("N,K,T,G,sym", [(300, 384, 100, 128, False), (256, 512, 129, 64, False),
+                                         (512, 512, 64, 128, True), (1, 128, 1, 128, False),
+                                         (17, 256, 300, 64, True)])
+def test_search_ragged(N, K, T, G, sym):
+    d = layer(N + K + T, N, K, T, n_out=max(1, K // 100))
+    _check_search(d["W"], d["X"], synth.alpha_grid(20), G, sym, use_m=True)
+
+
+def test_search_alpha_subsets():
+    d = layer(3, 256, 512, 96, n_out=4)
+    for alphas in ([0.0], [0.5, 0.25], np.linspace(0, 1, 64).astype(np.float32)):
+        _check_search(d["W"], d["X"], np.asarray(alphas, np.float32))
+
+
+def test_search_deterministic():
+    d = layer(4, 512, 1024, 512, n_out=8)
+    W, X = dev(d["W"]), dev(d["X"])
+    a = awq.search_scale(W, X, synth.alpha_grid(20))
+    b = awq.search_scale(W, X, synth.alpha_grid(20))
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+@pytest.mark.slow
+def test_search_full_size_llama7b_attn():
+    """K = N = 4096, T = 8192 (the benchmark's layer), in the benchmark's launch configuration:
+    the oracle's fp64 error at alpha_0 and at the chosen alpha, the codes of the chosen alpha,
+    and the argmin property over all 20."""
+    d = synth.make_layer("llama7b-attn-4096")
+    W16, X16 = d["W"], d["X"]
+    alphas = synth.alpha_grid(20)
+    W, X = dev(W16), dev(X16)
+    err, best, s, inv_s = awq.search_scale(W, X, alphas)
+    awq.awq_stream_status()
+    e = host(err).astype(np.float64)
+    b = int(host(best)[0])
+    assert b == int(np.argmin(e)) and np.all(np.isfinite(e))
+    s_b = host(s)
+    q, sc, z = awq.quantize_pack(W, s)
+    want = ref.quantize_pack(W16, s_b)
+    assert np.array_equal(host(q).view(np.uint32), want["qweight"])
+    e_b = ref.error_of_codes(X16, W16, want["qweight"], want["scales"], want["zeros"], s_b)
+    np.testing.assert_allclose(e[b], e_b, rtol=1e-3)
+    rtn = ref.quantize_pack(W16, None)
+    e_0 = ref.error_of_codes(X16, W16, rtn["qweight"], rtn["scales"], rtn["zeros"],
+                             np.ones(W16.shape[1], np.float32))
+    np.testing.assert_allclose(e[0], e_0, rtol=1e-3)
+    assert e[b] <= e[0]
+
+
+# ----------------------------------------------------------------------------- W4A16 matmul
+
+def _gemm_case(N, K, M, G, sym, with_inv, seed):
+    d = layer(seed, N, K, M, n_out=max(1, K // 64), mult=4.0)
+    W16, X16 = d["W"], d["X"]
+    rng = np.random.Generator(np.random.PCG64(seed + 1))
+    s = np.exp(rng.uniform(-0.5, 1.0, K)).astype(np.float32)
+    qd = ref.quantize_pack(W16, s, G, sym)
+    inv = (np.float32(1) / s).astype(np.float32) if with_inv else None
+    q = dev(qd["qweight"].view(np.int32))
+    Y = awq.w4a16_gemm(dev(X16), q, dev(qd["scales"]), dev(qd["zeros"]),
+                       dev(inv) if with_inv else None, G, sym)
+    awq.awq_stream_status()
+    want = ref.w4a16_gemm(X16, qd["qweight"], qd["scales"], qd["zeros"], G, inv_s=inv)
+    got = host(Y).astype(np.float64)
+    diff = np.abs(got - want)
+    rel = diff.max() / np.abs(want).max()
+    assert rel <= 2e-2, (N, K, M, G, sym, with_inv, rel)
+    return rel, np.quantile(diff / np.abs(want).max(), 0.999)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 32, 33, 64, 100, 128, 129, 256, 300])
+def test_w4a16_batch_sizes(M):
+    _gemm_case(384, 1152, M, 128, False, True, 100 + M)
+
+
+@pytest.mark.parametrize("N,K", [(512, 512), (300, 1152), (1, 128), (130, 64), (4096, 4096)])
+@pytest.mark.parametrize("M", [1, 8, 16, 128])
+@pytest.mark.parametrize("G,sym,with_inv", [(128, False, False), (64, False, True),
+                                            (128, True, True), (64, True, False)])
+def test_w4a16_shapes(N, K, M, G, sym, with_inv):
+    if K % G:
+        pytest.skip("K % G")
+    _gemm_case(N, K, M, G, sym, with_inv, N * 7 + K + M)
+
+
+def test_w4a16_large_k_chunked_gemv():
+    """K = 28672 at M = 8 stages the activations in several chunks."""
+    _gemm_case(64, 28672, 8, 128, False, True, 9)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 8, 64, 256, 1024])
+def test_w4a16_full_size_sampled(M):
+    """Llama-70B shapes (8192 -> 28672): 4096 sampled outputs, each computed by the oracle."""
+    N, K = 28672, 8192
+    rng = np.random.Generator(np.random.PCG64(M))
+    W16 = synth.draw_weight(rng, N, K, 0.01)
+    X16 = rng.standard_normal((M, K)).astype(np.float16)
+    s = np.exp(rng.uniform(-0.5, 1.0, K)).astype(np.float32)
+    q, sc, z = awq.quantize_pack(dev(W16), dev(s))
+    inv = (np.float32(1) / s).astype(np.float32)
+    Y = awq.w4a16_gemm(dev(X16), q, sc, z, dev(inv))
+    awq.awq_stream_status()
+    rows = rng.integers(0, M, 4096)
+    cols = rng.integers(0, N, 4096)
+    want = ref.w4a16_gemm_entries(X16, host(q).view(np.uint32), host(sc), host(z), rows, cols,
+                                  inv_s=inv)
+    got = host(Y)[rows, cols].astype(np.float64)
+    assert np.max(np.abs(got - want)) / np.max(np.abs(want)) <= 2e-2
+
+
+def test_w4a16_deterministic():
+    d = layer(8, 512, 1024, 128)
+    q, sc, z = awq.quantize_pack(dev(d["W"]))
+    X = dev(d["X"])
+    for M in (1, 128):
+        a = awq.w4a16_gemm(X[:M].contiguous(), q, sc, z)
+        b = awq.w4a16_gemm(X[:M].contiguous(), q, sc, z)
+        assert torch.equal(a, b)
