@@ -43,7 +43,7 @@ WORKLOAD = "llama7b-attn-4096"
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
@@ -80,6 +80,37 @@ def layer_units(wl_name):
     return wl, spec
 
 
+def profiled_traffic(profile_md, source):
+    """DRAM bytes per launch from a committed ncu summary, or None when the kernel source has
+    changed since the counters were taken (its sha256 prefix no longer matches)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", profile_md)
+    src = os.path.join(ROOT, "post_weight_quantization_stats_b300", "csrc", source)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    text = open(path).read()
+    want, traffic = None, None
+    for line in text.splitlines():
+        if line.startswith("source_sha256_16:"):
+            want = line.split(":", 1)[1].strip()
+        if line.startswith("| traffic_bytes_per_launch |"):
+            traffic = int(line.split("|")[2].strip())
+    return traffic if want == sha else None
+
+
+def layer_for_rank(wl_name, rank):
+    """The layer rank ``rank`` processes: rank 0 gets the workload's first layer; every other
+    rank an independent draw of the same shape (its own seed), so N ranks do N layers."""
+    wl = synth.WORKLOADS[wl_name]
+    if rank == 0:
+        return synth.make_layer(wl_name, 0)
+    if len(wl.layers) > 1:
+        return synth.make_layer(wl_name, rank % len(wl.layers))
+    own = synth.Workload(wl.wid * 100 + rank, wl.name, wl.layers, wl.gemm_m)
+    return synth.make_layer(own, 0)
+
+
 def algorithmic(spec, G, n_alpha, gemm_m):
     """Algorithmic bytes/flops per launch of each kernel for one layer (N, K, T)."""
     N, K, T = spec.n, spec.k, spec.t
@@ -109,6 +140,11 @@ class ClockSampler:
         self.path = None
 
     def start(self):
+        if self.bus_id:
+            probe = subprocess.run(["nvidia-smi", "-i", self.bus_id, "--query-gpu=index",
+                                    "--format=csv,noheader"], capture_output=True, text=True)
+            if probe.returncode != 0:
+                self.bus_id = None
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -386,10 +422,7 @@ def run_ours(args):
     awq.lib()
     peaks = measured_peaks()
     wl, spec = layer_units(args.workload)
-    layer = synth.make_layer(args.workload, rank % len(wl.layers) if len(wl.layers) > 1 else 0)
-    if rank > 0 and len(wl.layers) == 1:  # an independent layer per rank (own seed)
-        layer = synth.make_layer(synth.Workload(wl.wid * 100 + rank, wl.name, wl.layers,
-                                                wl.gemm_m), 0)
+    layer = layer_for_rank(args.workload, rank)
     dev = torch.device("cuda", local_rank)
     step = LayerStep(awq, torch, layer, wl, dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
@@ -448,7 +481,8 @@ def run_ours(args):
                 "achieved": round(achieved, 1) if achieved else None,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4) if achieved else None,
-                "traffic": None,
+                "traffic": profiled_traffic("score_kernel_llama7b_attn_4096.md", "score_gemm.cuh")
+                if args.workload == WORKLOAD else None,
                 "peak_note": f"{peaks['source']} dense bf16 burst (fp16 runs at the bf16 rate); "
                              f"sustained {peaks['bf16_tflops_sustained']}",
                 "flops_per_launch": alg["score"]["flops"]}
