@@ -146,6 +146,32 @@ uint64_t awq_launch_count(void);
  */
 uint64_t awq_set_wait_limit_ns(uint64_t limit_ns);
 
+/*
+ * The alpha search without any device allocation, for callers that cannot allocate device
+ * memory where they run it (a fixed memory budget set at start-up, a plug-in handed a device
+ * but no allocator, a process whose allocations belong to another runtime). The pages have no
+ * counterpart to this call; it exists only for such callers.
+ *
+ * Same arguments and results as awq_search_scale without the workspace: the scratch is a static
+ * device array of AWQ_SEARCH_STATIC_SCRATCH_BYTES (40 MiB) inside this library, which every GPU
+ * that loads the library holds until the process exits. Shapes whose
+ * awq_search_workspace_bytes(...) exceed it return AWQ_ERR_WORKSPACE without launching (the
+ * 4096 x 4096 layer with 20 alphas needs about 33 MiB). The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, which
+ * may load this library's device code on that device); make that first call before any stream
+ * capture. Every call shares the one array and leaves its contents behind; the search writes
+ * everything it later reads and clears its own max|W| word, so no clearing is needed between
+ * calls. Calls whose work overlaps on the GPU (for example on two streams at once) race on the
+ * array: serialise them.
+ */
+#define AWQ_SEARCH_STATIC_SCRATCH_BYTES (40u * 1024u * 1024u)
+awq_status_t awq_search_scale_static(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
+                                     int64_t T, const float* mean_abs, const float* alphas,
+                                     int32_t n_alpha, awq_qcfg_t cfg, float* err_out,
+                                     int32_t* best_idx, float* s_out, float* inv_s_out,
+                                     awq_stream_t stream);
+
 /* Kernels of this library, as counted by the profiling calls below. */
 typedef enum {
   AWQ_K_CALIB_STATS = 0, /* awq_calib_stats (and the search when mean_abs is NULL) */

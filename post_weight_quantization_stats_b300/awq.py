@@ -47,6 +47,9 @@ _SIGNATURES = {
     "awq_search_scale": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i64, _c_void_p,
                                         _c_void_p, _i32, QCfg, _c_void_p, _sz, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "awq_search_scale_static": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i64,
+                                               _c_void_p, _c_void_p, _i32, QCfg, _c_void_p,
+                                               _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "awq_quantize_pack": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, QCfg, _c_void_p,
                                          _c_void_p, _c_void_p, _c_void_p]),
     "awq_w4a16_gemm": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
@@ -131,6 +134,20 @@ def awq_search_scale(W, N, K, X, T, mean_abs, alphas, n_alpha, group_size, symme
         _ptr(W), N, K, _ptr(X), T, _ptr(mean_abs), ctypes.cast(arr, ctypes.c_void_p), n_alpha,
         _cfg(group_size, symmetric), _ptr(workspace), ws_bytes, _ptr(err_out), _ptr(best_idx),
         _ptr(s_out), _ptr(inv_s_out), _stream(stream)))
+
+
+def awq_search_scale_static(W, N, K, X, T, mean_abs, alphas, n_alpha, group_size, symmetric,
+                            err_out, best_idx, s_out, inv_s_out, stream=None):
+    """The alpha search with the library's static scratch array instead of a workspace, for
+    callers that cannot allocate device memory (see include/awq.h). Allocates nothing."""
+    arr = (ctypes.c_float * int(n_alpha))(*[float(a) for a in alphas])
+    _check("awq_search_scale_static", lib().awq_search_scale_static(
+        _ptr(W), N, K, _ptr(X), T, _ptr(mean_abs), ctypes.cast(arr, ctypes.c_void_p), n_alpha,
+        _cfg(group_size, symmetric), _ptr(err_out), _ptr(best_idx), _ptr(s_out),
+        _ptr(inv_s_out), _stream(stream)))
+
+
+SEARCH_STATIC_SCRATCH_BYTES = 40 * 1024 * 1024
 
 
 def awq_quantize_pack(W, N, K, s, group_size, symmetric, qweight, scales, zeros, stream=None):

@@ -42,7 +42,7 @@ def build(force: bool = False, ptxas_info: bool = False, verbose: bool = False) 
         return LIB
     cmd = [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "-I", os.path.join(ROOT, "include"), "-o", LIB + ".tmp",
-           os.path.join(CSRC, "awq_api.cu")]
+           os.path.join(CSRC, "awq_api.cu"), os.path.join(CSRC, "awq_static_scratch.cu")]
     if ptxas_info:
         cmd.insert(1, "-Xptxas=-v")
     if verbose:
