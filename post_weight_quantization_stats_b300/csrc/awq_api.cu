@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/awq.h"
@@ -181,6 +182,42 @@ awq_status_t make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
   return r == CUDA_SUCCESS ? AWQ_OK : AWQ_ERR_CUDA;
 }
 
+// 2-D tensor map of a row-major [rows, cols] matrix of `elem_bytes`-byte elements (row stride
+// `ld` elements), box [box_rows, box_cols], no swizzle unless asked, out-of-range elements read
+// as zero.
+awq_status_t make_map_plain(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes,
+                            const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                            int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * static_cast<cuuint64_t>(elem_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
+// Launch with a cluster of `cz` CTAs along grid z (cz = 1: a plain launch).
+template <typename... P, typename... A>
+awq_status_t launch_k(void (*kern)(P...), dim3 grid, int threads, size_t smem, int cz,
+                      cudaStream_t st, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = static_cast<unsigned>(cz);
+  cfg.attrs = attr;
+  cfg.numAttrs = cz > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...) != cudaSuccess) return AWQ_ERR_CUDA;
+  return AWQ_OK;
+}
+
 // ------------------------------------------------------------------ launch helpers
 
 awq_status_t launch_calib_stats(const __half* X, int64_t T, int64_t K, int64_t ldx, float* m,
@@ -207,52 +244,118 @@ awq_status_t launch_quantize_pack(const __half* W, int64_t N, int64_t K, const f
   return launched(AWQ_K_QUANTIZE_PACK, st);
 }
 
-template <int BN, int G, bool INV>
-awq_status_t launch_tc_t(const CUtensorMap& map, const w4tc::Args& a, cudaStream_t st) {
-  auto kern = w4tc::w4a16_tc_kernel<BN, G, INV>;
-  constexpr int smem = w4tc::Cfg<BN>::SMEM;
+// Tensor-core W4A16, grouped kernel (M <= 16): 120-row tiles, K split over a cluster of up
+// to 8 CTAs (whole groups each) so the tiles fill two CTAs per SM.
+awq_status_t launch_w4_grouped(const __half* X, const w4tc::Args& a0, int G, int sms,
+                               cudaStream_t st) {
+  namespace gk = w4tc::grouped;
+  w4tc::Args a = a0;
+  const int tiles = (a.N + gk::ROWS - 1) / gk::ROWS;
+  const int nraw = (a.K + gk::RK - 1) / gk::RK;   // K splits are whole 256-channel raw stages
+  int splits = 1;
+  for (int sp = 1; sp <= 8; ++sp)
+    if (tiles * sp <= 2 * sms && sp <= nraw) splits = sp;
+  a.splits = splits;
+  CUtensorMap mq, mx;
+  const int mt = a.M <= 1 ? 1 : a.M <= 2 ? 2 : a.M <= 4 ? 4 : a.M <= 8 ? 8 : 16;
+  AWQ_TRY(make_map_plain(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a.Q, a.N, a.K / 8, a.K / 8,
+                         gk::RK / 8, gk::ROWS, CU_TENSOR_MAP_SWIZZLE_128B));
+  AWQ_TRY(make_map_plain(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, X, a.M, a.K, a.K, gk::RK, mt));
+  using KernT = void (*)(CUtensorMap, CUtensorMap, w4tc::Args);
+  KernT kern;
+  if (G == 128)
+    kern = mt == 1 ? gk::grouped_kernel<128, 1> : mt == 2 ? gk::grouped_kernel<128, 2>
+         : mt == 4 ? gk::grouped_kernel<128, 4> : mt == 8 ? gk::grouped_kernel<128, 8>
+                   : gk::grouped_kernel<128, 16>;
+  else
+    kern = mt == 1 ? gk::grouped_kernel<64, 1> : mt == 2 ? gk::grouped_kernel<64, 2>
+         : mt == 4 ? gk::grouped_kernel<64, 4> : mt == 8 ? gk::grouped_kernel<64, 8>
+                   : gk::grouped_kernel<64, 16>;
+  const int smem = gk::smem_bytes(mt);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
     return AWQ_ERR_CUDA;
   }
-  dim3 grid(static_cast<unsigned>((a.N + w4tc::BM - 1) / w4tc::BM),
-            static_cast<unsigned>((a.M + BN - 1) / BN));
   prof_start(AWQ_K_GEMM_TC, st);
-  kern<<<grid, w4tc::THREADS, smem, st>>>(map, a);
-  return launched(AWQ_K_GEMM_TC, st);
+  const awq_status_t rc = launch_k(kern, dim3(static_cast<unsigned>(tiles), 1, static_cast<unsigned>(splits)),
+                                   w4tc::THREADS, static_cast<size_t>(smem), splits, st, mq, mx, a);
+  const awq_status_t rl = launched(AWQ_K_GEMM_TC, st);
+  return rc != AWQ_OK ? rc : rl;
 }
 
+// Tensor-core W4A16, dequant kernel (any M; used above 16 tokens): token tile BN by M, K split
+// over a cluster while the tiles alone leave SMs idle (each CTA keeps >= 2 stages).
 template <int BN>
-awq_status_t launch_tc_bn(const __half* X, const w4tc::Args& a, int G, bool inv, cudaStream_t st) {
-  CUtensorMap map;
-  AWQ_TRY(make_map(&map, X, a.M, a.K, a.K, BN));
-  if (G == 128)
-    return inv ? launch_tc_t<BN, 128, true>(map, a, st) : launch_tc_t<BN, 128, false>(map, a, st);
-  return inv ? launch_tc_t<BN, 64, true>(map, a, st) : launch_tc_t<BN, 64, false>(map, a, st);
+awq_status_t launch_w4_dequant_bn(const __half* X, const w4tc::Args& a0, int G, int sms,
+                                  cudaStream_t st) {
+  namespace dk = w4tc::dequant;
+  using C = dk::Cfg<BN>;
+  w4tc::Args a = a0;
+  const int tiles_n = (a.N + w4tc::BM - 1) / w4tc::BM, tiles_m = (a.M + BN - 1) / BN;
+  const int nkb = (a.K + dk::BK - 1) / dk::BK;
+  int splits = 1;
+  for (int sp = 1; sp <= 8; ++sp)
+    if (tiles_n * tiles_m * sp <= sms && nkb >= 2 * sp) splits = sp;
+  a.splits = splits;
+  CUtensorMap mq, mx;
+  AWQ_TRY(make_map_plain(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a.Q, a.N, a.K / 8, a.K / 8,
+                         dk::BK / 8, w4tc::BM));
+  AWQ_TRY(make_map(&mx, X, a.M, a.K, a.K, BN));
+  auto kern = G == 128 ? dk::dequant_kernel<BN, 128> : dk::dequant_kernel<BN, 64>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) {
+    cudaGetLastError();
+    return AWQ_ERR_CUDA;
+  }
+  prof_start(AWQ_K_GEMM_TC, st);
+  const awq_status_t rc = launch_k(kern, dim3(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m),
+                                              static_cast<unsigned>(splits)),
+                                   w4tc::THREADS, static_cast<size_t>(C::SMEM), splits, st, mq, mx, a);
+  const awq_status_t rl = launched(AWQ_K_GEMM_TC, st);
+  return rc != AWQ_OK ? rc : rl;
+}
+
+awq_status_t launch_w4_dequant(const __half* X, const w4tc::Args& a, int G, int sms, cudaStream_t st) {
+  if (a.M <= 32) return launch_w4_dequant_bn<32>(X, a, G, sms, st);
+  if (a.M <= 64) return launch_w4_dequant_bn<64>(X, a, G, sms, st);
+  if (a.M <= 128) return launch_w4_dequant_bn<128>(X, a, G, sms, st);
+  return launch_w4_dequant_bn<256>(X, a, G, sms, st);
+}
+
+// Launch shape of the decode GEMV: one CTA per SM (at most one per output row); the K parts
+// follow from the items each lane holds; a stage holds at least one row per row group and about
+// 32 KB; the ring is as deep as shared memory allows (at least 2 stages). Shapes that do not fit
+// (K above 32 * 32 * IPL * CWARPS channels, or too many group parameters per CTA) return
+// AWQ_ERR_UNSUPPORTED_SHAPE and go to the tensor-core kernel instead.
+awq_status_t gemv_shape(gemv::Args& a, int G, int sms) {
+  const int grid = static_cast<int>(std::min<int64_t>(sms, a.N));
+  a.rows_max = (a.N + grid - 1) / grid;
+  const int ipl = gemv::items_per_lane(a.M);
+  const int items = a.K / gemv::ITEM_CH;
+  a.parts = (items + 32 * ipl - 1) / (32 * ipl);
+  if (a.parts > gemv::CWARPS) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  a.row_groups = gemv::CWARPS / a.parts;
+  const int row_bytes = a.K / 2;
+  a.rows_stage = std::max(a.row_groups, (32768 / row_bytes) / a.row_groups * a.row_groups);
+  a.stage_bytes = a.rows_stage * row_bytes;
+  a.pstride = a.K / G + 1;
+  a.nstages = gemv::MAX_STAGES;
+  while (a.nstages > 2 && gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) --a.nstages;
+  if (gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  return AWQ_OK;
 }
 
 template <int M>
-awq_status_t launch_gemv_m(const gemv::Args& a0, int G, int sms, cudaStream_t st) {
-  gemv::Args a = a0;
-  const int64_t grid = std::min<int64_t>(2 * static_cast<int64_t>(sms),
-                                         std::max<int64_t>(1, (a.N + gemv::R - 1) / gemv::R));
-  a.rows_max = static_cast<int>((a.N + grid - 1) / grid) + 1;
-  const int64_t ysum_bytes = static_cast<int64_t>(a.rows_max) * M * 4;
-  const int64_t budget = 100 * 1024 - ysum_bytes;
-  int64_t kc = (budget / (2 * M)) / gemv::STEP_K * gemv::STEP_K;
-  const int64_t kpad = (a.K + gemv::STEP_K - 1) / gemv::STEP_K * gemv::STEP_K;
-  if (kc > kpad) kc = kpad;
-  if (kc < gemv::STEP_K) kc = gemv::STEP_K;
-  a.kc = static_cast<int>(kc);
-  const size_t smem = static_cast<size_t>(M) * kc * 2 + static_cast<size_t>(ysum_bytes);
+awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
+  const size_t smem = gemv::smem_bytes(a);
   auto kern = (G == 128) ? gemv::gemv_kernel<M, 128> : gemv::gemv_kernel<M, 64>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return AWQ_ERR_CUDA;
   }
+  const unsigned grid = static_cast<unsigned>((a.N + a.rows_max - 1) / a.rows_max);
   prof_start(AWQ_K_GEMV, st);
-  kern<<<static_cast<unsigned>(grid), gemv::THREADS, smem, st>>>(a);
+  kern<<<grid, gemv::THREADS, smem, st>>>(a);
   return launched(AWQ_K_GEMV, st);
 }
 
@@ -537,32 +640,37 @@ awq_status_t awq_w4a16_gemm(const void* X_f16, int64_t M, int64_t N, int64_t K,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const uint8_t* z = cfg.symmetric ? nullptr : zeros;
   const int G = cfg.group_size;
-  if (M <= 8) {
-    gemv::Args a{static_cast<const __half*>(X_f16), qweight, static_cast<const __half*>(scales_f16),
-                 z, inv_s, static_cast<__half*>(Y_f16), static_cast<int>(M), static_cast<int>(N),
-                 static_cast<int>(K), 0, 0};
-    switch (M) {
-      case 1: return launch_gemv_m<1>(a, G, d->sms, st);
-      case 2: return launch_gemv_m<2>(a, G, d->sms, st);
-      case 3: return launch_gemv_m<3>(a, G, d->sms, st);
-      case 4: return launch_gemv_m<4>(a, G, d->sms, st);
-      case 5: return launch_gemv_m<5>(a, G, d->sms, st);
-      case 6: return launch_gemv_m<6>(a, G, d->sms, st);
-      case 7: return launch_gemv_m<7>(a, G, d->sms, st);
-      default: return launch_gemv_m<8>(a, G, d->sms, st);
-    }
+  if (M <= gemv::MAX_M) {
+    gemv::Args a{};
+    a.X = static_cast<const __half*>(X_f16);
+    a.Q = qweight;
+    a.scales = static_cast<const __half*>(scales_f16);
+    a.zeros = z;
+    a.inv_s = inv_s;
+    a.Y = static_cast<__half*>(Y_f16);
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.status = d->status;
+    a.limit_ns = g_wait_limit_ns.load();
+    if (gemv_shape(a, G, d->sms) == AWQ_OK)
+      return M == 1 ? launch_gemv_m<1>(a, G, st) : launch_gemv_m<2>(a, G, st);
   }
-  w4tc::Args a{qweight, static_cast<const __half*>(scales_f16), z, inv_s,
-               static_cast<__half*>(Y_f16), static_cast<int>(M), static_cast<int>(N),
-               static_cast<int>(K), static_cast<int>((K + w4tc::BK - 1) / w4tc::BK), d->status,
-               g_wait_limit_ns.load()};
+  w4tc::Args a{};
+  a.Q = qweight;
+  a.scales = static_cast<const __half*>(scales_f16);
+  a.zeros = z;
+  a.inv_s = inv_s;
+  a.Y = static_cast<__half*>(Y_f16);
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.splits = 1;
+  a.status = d->status;
+  a.limit_ns = g_wait_limit_ns.load();
   const __half* X = static_cast<const __half*>(X_f16);
-  const bool inv = inv_s != nullptr;
-  if (M <= 16) return launch_tc_bn<16>(X, a, G, inv, st);
-  if (M <= 32) return launch_tc_bn<32>(X, a, G, inv, st);
-  if (M <= 64) return launch_tc_bn<64>(X, a, G, inv, st);
-  if (M <= 128) return launch_tc_bn<128>(X, a, G, inv, st);
-  return launch_tc_bn<256>(X, a, G, inv, st);
+  if (M <= w4tc::grouped::BN) return launch_w4_grouped(X, a, G, d->sms, st);
+  return launch_w4_dequant(X, a, G, d->sms, st);
 }
 
 }  // extern "C"
