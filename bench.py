@@ -7,9 +7,11 @@ projection (K = N = 4096, T = 8192 calibration tokens, 20 alphas, group 128):
   argmin) -> final quantise/pack -> W4A16 matmul at M = 1, 4, 16, 128.
 Inputs are resident in HBM when the timed region starts; L2 is flushed (256 MB write) between
 steps, outside the per-step CUDA events. The headline is layers/s; the JSON line also carries the
-roofline of the dominant kernel (the scoring GEMM), per-kernel live timings, an HBM-bound W4A16
-sweep over weight sets larger than L2, the end-to-end number through host buffers, the CPU
-oracle baseline and the SM clocks seen during the timed region.
+roofline of the dominant kernel (the scoring GEMM), per-kernel live timings, a W4A16 sweep
+(CUDA-graph replays over weight sets larger than L2, on this layer and the Llama-70B MLP shapes)
+with its decode (HBM) and M=1024 (tensor) rooflines, one decode step through all 224 linears of
+the synthetic 7B stack, the end-to-end number through host buffers, the CPU oracle baseline and
+the SM clocks seen during the timed region (NVML, every ~10 ms).
 
 ``--impl reference`` times the CPU oracle instead (bounded samples of the same layer).
 Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under torchrun, every rank
@@ -50,6 +52,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hbm-sweep", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="run one kernel family on a small case and exit (for profiler "
+                         "captures): 'search' (statistic, alpha search and pack of the "
+                         "workload's layer, 3 times) or 'w4a16:N:K:M' (4 launches of one shape)")
     return ap.parse_args(argv)
 
 
@@ -174,6 +180,98 @@ class ClockSampler:
                         rows.append(parts)
             os.unlink(self.path)
         return summarize_clocks(rows)
+
+
+class NvmlClockSampler:
+    """SM clock, max clock, power and clock-event reasons read through NVML every ~10 ms on a
+    background thread (many samples even for a timed region of a few hundred ms). Produces the
+    same rows as ClockSampler; raises if NVML is unavailable."""
+
+    # NVML clock-event reason bits (nvml.h): sw power cap, hw slowdown, sw / hw thermal slowdown
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, bus_id=None, period_s=0.01):
+        import ctypes
+        self.ct = ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")   # the driver's NVML (read-only queries)
+        self.nv = nv
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        rc = -1
+        if bus_id:
+            rc = nv.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(h))
+        if rc != 0 and nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML device handle")
+        self.h = h
+        self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.period = period_s
+        self.rows = []
+        self._stop = None
+        self._thread = None
+
+    def _query(self):
+        ct, nv = self.ct, self.nv
+        sm, mx, pw, r = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ct.byref(sm)) or
+                nv.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM, ct.byref(mx)) or
+                nv.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw)) or
+                self.reasons_fn(self.h, ct.byref(r))):
+            return None
+        return sm.value, mx.value, pw.value / 1000.0, r.value
+
+    def _loop(self):
+        while not self._stop.is_set():
+            q = self._query()
+            if q is not None:
+                sm, mx, pw, r = q
+                act = ["Active" if r & self.BITS[k] else "Not Active"
+                       for k in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                 "sw_power_cap")]
+                self.rows.append(["0", str(sm), str(mx), f"{pw:.1f}", hex(r)] + act)
+            self._stop.wait(self.period)
+
+    def start(self):
+        import threading
+        if self._query() is None:
+            raise RuntimeError("NVML queries failed")
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+        return self
+
+    def stop(self):
+        self._stop.set()
+        self._thread.join(timeout=5)
+        out = summarize_clocks(self.rows)
+        out["source"] = "nvml"
+        return out
+
+
+class _FallbackSampler(ClockSampler):
+    """The nvidia-smi sampler, recording why NVML could not be used."""
+
+    def __init__(self, bus_id, reason):
+        super().__init__(bus_id)
+        self.reason = reason
+
+    def stop(self):
+        out = super().stop()
+        out["source"] = "nvidia-smi"
+        out["nvml_error"] = self.reason
+        return out
+
+
+def clock_sampler(bus_id):
+    """NVML sampler when NVML works, else the nvidia-smi one."""
+    try:
+        return NvmlClockSampler(bus_id).start()
+    except Exception as e:  # noqa: BLE001
+        return _FallbackSampler(bus_id, f"{type(e).__name__}: {e}"[:200]).start()
 
 
 def summarize_clocks(rows):
@@ -363,48 +461,115 @@ class LayerStep:
             [self.ym[M] for M in self.gemm_m]
 
 
-def hbm_sweep(awq, torch, N, K, G, ms, peaks, reps=20):
-    """W4A16 at each M over weight sets whose total exceeds 2x L2, so every launch streams its
-    weights from HBM. Per-launch time from the library's event pairs."""
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size if hasattr(
-        torch.cuda.get_device_properties(0), "L2_cache_size") else 126 * 2 ** 20
-    packed = N * K // 2 + 3 * N * (K // G)
-    copies = int(max(2, -(-2 * l2 // packed)))
+def w4a16_graph_time(awq, torch, N, K, G, M, sets, inv, reps_outer=3):
+    """Per-launch time (us) of awq_w4a16_gemm at [M, K] x [N, K]^T, from a CUDA graph that walks
+    rotating weight sets (more bytes than L2, so each launch streams its weights from HBM):
+    events around whole graph replays, no host work inside the timed region."""
+    X = torch.randn((M, K), device="cuda").half()
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    for q, sc, z in sets:   # non-captured first launches (kernel attributes, module load)
+        awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y)
+    awq.awq_stream_status()
+    per_graph = max(len(sets), 24 // max(1, len(sets)) * len(sets))
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(per_graph):
+                q, sc, z = sets[i % len(sets)]
+                awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y, stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps_outer):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    awq.awq_stream_status()
+    return e0.elapsed_time(e1) * 1e3 / (reps_outer * per_graph)
+
+
+def w4a16_sweep(awq, torch, shapes, ms, G, peaks):
+    """W4A16 throughput per (shape, M): HBM GB/s of the algorithmic bytes (packed weights +
+    metadata + activations + outputs + inv_s) and TFLOP/s, each against the measured peaks."""
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
     gen = torch.Generator(device="cuda").manual_seed(7)
-    sets = []
-    for _ in range(copies):
-        q = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32, device="cuda",
-                          generator=gen)
-        sc = (torch.rand((K // G, N), device="cuda", generator=gen) * 0.01 + 1e-3).half()
-        z = torch.randint(0, 16, (K // G, N), dtype=torch.uint8, device="cuda", generator=gen)
-        sets.append((q, sc, z))
     out = []
-    for M in ms:
-        X = (torch.randn((M, K), device="cuda", generator=gen)).half()
-        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
-        for i in range(copies):  # warm-up (code paths, TMA descriptors)
-            q, sc, z = sets[i]
-            awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, None, G, False, Y)
-        torch.cuda.synchronize()
-        awq.awq_profile_begin()
-        for r in range(reps):
-            for i in range(copies):
-                q, sc, z = sets[i]
-                awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, None, G, False, Y)
-        prof = awq.awq_profile_end()
-        name = "gemv" if M <= 8 else "gemm_tc"
-        n, ms_tot = prof[name]
-        us = ms_tot * 1e3 / n
-        byts = packed + 2 * M * K + 2 * M * N
-        gbs = byts / (us * 1e-6) / 1e9
-        tfl = 2 * M * N * K / (us * 1e-6) / 1e12
-        out.append({"M": M, "N": N, "K": K, "kernel": name, "us": round(us, 3),
-                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                    "TFLOP/s": round(tfl, 2), "frac_tensor": round(tfl / peaks["bf16_tflops"], 4),
-                    "weight_sets": copies})
-    del sets
-    torch.cuda.empty_cache()
+    for N, K in shapes:
+        packed = N * K // 2 + 3 * N * (K // G)
+        copies = int(max(2, -(-2 * l2 // packed)))
+        sets = [(torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32,
+                               device="cuda", generator=gen),
+                 (torch.rand((K // G, N), device="cuda", generator=gen) * 0.01 + 1e-3).half(),
+                 torch.randint(0, 16, (K // G, N), dtype=torch.uint8, device="cuda",
+                               generator=gen))
+                for _ in range(copies)]
+        inv = torch.rand(K, device="cuda", generator=gen) + 0.5
+        for M in ms:
+            us = w4a16_graph_time(awq, torch, N, K, G, M, sets, inv)
+            byts = packed + 2 * M * K + 2 * M * N + 4 * K
+            gbs = byts / (us * 1e-6) / 1e9
+            tfl = 2 * M * N * K / (us * 1e-6) / 1e12
+            out.append({"N": N, "K": K, "M": M,
+                        "kernel": "gemv" if M <= 2 else ("grouped_tc" if M <= 16 else "dequant_tc"),
+                        "us": round(us, 3), "GB/s": round(gbs, 1),
+                        "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                        "TFLOP/s": round(tfl, 2),
+                        "frac_tensor": round(tfl / peaks["bf16_tflops"], 4),
+                        "weight_sets": copies, "timing": "CUDA graph replay, L2-cold weights"})
+        del sets
+        torch.cuda.empty_cache()
     return out
+
+
+def stack_decode(awq, torch, peaks, G=128, M=1):
+    """One decode step (M tokens) through all 224 linears of the synthetic 7B stack, captured in
+    one CUDA graph: weight bytes streamed per token against the HBM peak."""
+    wl = synth.WORKLOADS["llama7b-stack"]
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    layers = []
+    total = 0
+    for spec in wl.layers:
+        N, K = spec.n, spec.k
+        layers.append((N, K,
+                       torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32,
+                                     device="cuda", generator=gen),
+                       (torch.rand((K // G, N), device="cuda", generator=gen) * 0.01 + 1e-3).half(),
+                       torch.randint(0, 16, (K // G, N), dtype=torch.uint8, device="cuda",
+                                     generator=gen),
+                       torch.randn((M, K), device="cuda", generator=gen).half(),
+                       torch.empty((M, N), dtype=torch.float16, device="cuda"),
+                       torch.rand(K, device="cuda", generator=gen) + 0.5))
+        total += N * K // 2 + 3 * N * (K // G) + 2 * M * K + 2 * M * N + 4 * K
+    for N, K, q, sc, z, X, Y, inv in layers[:7]:
+        awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y)
+    awq.awq_stream_status()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for N, K, q, sc, z, X, Y, inv in layers:
+                awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y, stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    awq.awq_stream_status()
+    ms = e0.elapsed_time(e1) / reps
+    gbs = total / (ms * 1e-3) / 1e9
+    del layers
+    torch.cuda.empty_cache()
+    return {"linears": len(wl.layers), "M": M, "group_size": G, "ms_per_token_step": round(ms, 4),
+            "tokens_per_s": round(M / (ms * 1e-3), 1), "bytes_per_step": total,
+            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "roofline_ms": round(total / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
+            "timing": "one CUDA graph of all linears, weights streamed from HBM"}
 
 
 def run_ours(args):
@@ -436,7 +601,7 @@ def run_ours(args):
     if hasattr(props, "pci_bus_id"):
         bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:" \
               f"{getattr(props, 'pci_device_id', 0):02X}.0"
-    clocks = ClockSampler(bus).start()
+    clocks = clock_sampler(bus)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier(world)
@@ -502,12 +667,22 @@ def run_ours(args):
         "wall_s_timed": round(t_wall, 4),
     }
     if rank == 0 and not args.no_hbm_sweep:
-        line["w4a16_hbm"] = hbm_sweep(awq, torch, step.N, step.K, step.G, step.gemm_m, peaks)
-        g1 = [r for r in line["w4a16_hbm"] if r["M"] == 1]
-        if g1:
-            line["roofline_gemv_m1"] = {"bound": "hbm", "achieved": g1[0]["GB/s"],
-                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                        "frac": g1[0]["frac_hbm"], "traffic": None}
+        shapes = [(step.N, step.K), (28672, 8192), (8192, 28672)]
+        line["w4a16"] = w4a16_sweep(awq, torch, shapes, sorted(set(step.gemm_m) | {1, 16, 1024}),
+                                    step.G, peaks)
+        dec = [r for r in line["w4a16"] if r["M"] == 1 and r["N"] == 28672]
+        pre = [r for r in line["w4a16"] if r["M"] == 1024 and r["N"] == 28672]
+        if dec:
+            line["roofline_w4a16_decode"] = {
+                "bound": "hbm", "kernel": dec[0]["kernel"], "shape": "M=1, 8192 -> 28672",
+                "achieved": dec[0]["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dec[0]["frac_hbm"], "traffic": None}
+        if pre:
+            line["roofline_w4a16_gemm"] = {
+                "bound": "tensor", "kernel": pre[0]["kernel"], "shape": "M=1024, 8192 -> 28672",
+                "achieved": pre[0]["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": pre[0]["frac_tensor"], "traffic": None}
+        line["w4a16_stack_decode"] = stack_decode(awq, torch, peaks)
     if not args.no_e2e:
         line["e2e"] = e2e_run(awq, torch, step, layer, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -551,10 +726,44 @@ def e2e_run(awq, torch, step, layer, args, world):
             "d2h_bytes_per_step": d2h}
 
 
+def run_case(args):
+    """One kernel family on a small case, for profiler captures (no timing, no JSON line)."""
+    import torch
+
+    from post_weight_quantization_stats_b300 import awq
+
+    torch.cuda.set_device(0)
+    awq.lib()
+    if args.case == "search":
+        wl, _ = layer_units(args.workload)
+        step = LayerStep(awq, torch, synth.make_layer(args.workload, 0), wl, torch.device("cuda", 0))
+        for _ in range(3):
+            step.enqueue()
+    elif args.case.startswith("w4a16:"):
+        N, K, M = (int(v) for v in args.case.split(":")[1:4])
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        q = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32, device="cuda",
+                          generator=gen)
+        sc = (torch.rand((K // 128, N), device="cuda", generator=gen) * 0.01 + 1e-3).half()
+        z = torch.randint(0, 16, (K // 128, N), dtype=torch.uint8, device="cuda", generator=gen)
+        inv = torch.rand(K, device="cuda", generator=gen) + 0.5
+        X = torch.randn((M, K), device="cuda", generator=gen).half()
+        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        for _ in range(4):
+            awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, 128, False, Y)
+    else:
+        raise SystemExit(f"bench.py: unknown --case {args.case}")
+    awq.awq_stream_status()
+    print(f"case {args.case} ok")
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
     return run_ours(args)
 
 

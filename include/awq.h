@@ -62,7 +62,7 @@ typedef enum {
   AWQ_ERR_INVALID_ARG = 1,       /* NULL pointer, non-positive size, bad group size/alpha count */
   AWQ_ERR_UNSUPPORTED_SHAPE = 2, /* K % G != 0, ldx < K or not a multiple of 8, size limits */
   AWQ_ERR_MISALIGNED = 3,        /* a device pointer is not 16-byte aligned */
-  AWQ_ERR_WORKSPACE = 4,         /* workspace NULL or smaller than awq_search_workspace_bytes */
+  AWQ_ERR_WORKSPACE = 4,         /* workspace NULL or below the one-buffer search workspace */
   AWQ_ERR_CUDA = 5,              /* a CUDA runtime/driver call or kernel launch failed */
   AWQ_ERR_TIMEOUT = 6,           /* a device-side bounded wait gave up (see awq_stream_status) */
   AWQ_ERR_NO_DEVICE = 7          /* no usable device, or the device is not sm_103 */
@@ -82,7 +82,13 @@ typedef struct {
 awq_status_t awq_calib_stats(const void* X_f16, int64_t T, int64_t K, int64_t ldx,
                              float* mean_abs, awq_stream_t stream);
 
-/* Bytes of device workspace awq_search_scale needs for this shape (0 on invalid input). */
+/*
+ * Bytes of device workspace for awq_search_scale's fastest schedule (0 on invalid input): two
+ * residual buffers, so the next alpha candidate's residual is built while the current one is
+ * scored. awq_search_scale also accepts less, down to one residual buffer (this value minus
+ * 2 N K bytes rounded up to 256), and then scores the candidates strictly one after the other
+ * (same results, bit for bit).
+ */
 size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
                                   awq_qcfg_t cfg);
 
@@ -92,13 +98,19 @@ size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alp
  *   X_f16    [T, K] fp16 row-major: calibration activations
  *   mean_abs [K] fp32 statistic from awq_calib_stats, or NULL to compute it here
  *   alphas   host [n_alpha] fp32 exponents (1 <= n_alpha <= 64), e.g. i/20 for i < 20
- *   workspace / ws_bytes   device scratch of at least awq_search_workspace_bytes(...)
+ *   workspace / ws_bytes   device scratch: awq_search_workspace_bytes(...) bytes, or at least
+ *                          the one-buffer size given there
  *   err_out  [n_alpha] fp32 out: E(alpha_i)
  *   best_idx [1] int32 out: first i with the smallest E (computed in fp64)
  *   s_out    [K] fp32 out (may be NULL): s = max(m, 1e-6)^alpha* as used for the codes
  *   inv_s_out[K] fp32 out (may be NULL): 1 / s (IEEE division), the GEMM's inv_s
  * The scales are computed in fp64 and rounded to fp32; the codes behind E(alpha_i) are exactly
  * those awq_quantize_pack produces for s_i.
+ * With the two-buffer workspace, the residual kernels run on a second stream owned by the
+ * library (one per device, created on the first call on that device together with the events
+ * that order it); it forks from `stream` and rejoins it before the call's last kernel, so the
+ * whole sequence can be captured in a CUDA graph once that first call has been made. Searches
+ * issued concurrently on one device serialise their residual kernels on that stream.
  */
 awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
                               int64_t T, const float* mean_abs, const float* alphas,
@@ -154,9 +166,10 @@ uint64_t awq_set_wait_limit_ns(uint64_t limit_ns);
  *
  * Same arguments and results as awq_search_scale without the workspace: the scratch is a static
  * device array of AWQ_SEARCH_STATIC_SCRATCH_BYTES (40 MiB) inside this library, which every GPU
- * that loads the library holds until the process exits. Shapes whose
- * awq_search_workspace_bytes(...) exceed it return AWQ_ERR_WORKSPACE without launching (the
- * 4096 x 4096 layer with 20 alphas needs about 33 MiB). The call allocates nothing.
+ * that loads the library holds until the process exits. Shapes whose smallest workspace (one
+ * residual buffer, see awq_search_workspace_bytes) exceeds it return AWQ_ERR_WORKSPACE without
+ * launching (the 4096 x 4096 layer with 20 alphas needs about 33 MiB); shapes that fit twice
+ * over use the overlapped schedule. The call allocates nothing.
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, which
  * may load this library's device code on that device); make that first call before any stream

@@ -38,6 +38,10 @@ struct DeviceInfo {
   bool ok = false;
   int sms = 0;
   int* status = nullptr;
+  // the search's second stream (residuals run there, overlapping the scoring GEMM) and the
+  // events that order the two streams; created once, on the first call on this device
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, res_done[2] = {nullptr, nullptr}, score_done[2] = {nullptr, nullptr};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -84,6 +88,15 @@ awq_status_t device_info(DeviceInfo** out) {
         return AWQ_ERR_CUDA;
       }
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.res_done[0], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.res_done[1], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.score_done[0], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.score_done[1], cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return AWQ_ERR_CUDA;
     }
     d.ok = true;
   }
@@ -234,8 +247,8 @@ awq_status_t launch_quantize_pack(const __half* W, int64_t N, int64_t K, const f
                                   cudaStream_t st) {
   QuantArgs a{W, s, q, scales, cfg.symmetric ? nullptr : zeros, static_cast<int>(N),
               static_cast<int>(K), cfg.symmetric};
-  const int64_t words = N * (K / 8);
-  const unsigned grid = static_cast<unsigned>((words + 255) / 256);
+  const dim3 grid(static_cast<unsigned>((N + 8 * QROWS - 1) / (8 * QROWS)),
+                  static_cast<unsigned>((K / 8 + 31) / 32));
   prof_start(AWQ_K_QUANTIZE_PACK, st);
   if (cfg.group_size == 128)
     quantize_pack_kernel<128><<<grid, 256, 0, st>>>(a);
@@ -395,7 +408,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, in
 }
 
 struct SearchLayout {
-  size_t m, s_grid, inv_grid, absmax, partial, D, total;
+  size_t m, s_grid, inv_grid, absmax, partial, D, D2, min_total, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -409,7 +422,9 @@ SearchLayout search_layout(int64_t N, int64_t K, int32_t n_alpha) {
   L.absmax = off;   off = align256(off + sizeof(unsigned int));
   L.partial = off;  off = align256(off + sizeof(double) * kPartialStride * n_alpha);
   L.D = off;        off = align256(off + sizeof(__half) * N * K);
-  L.total = off;
+  L.min_total = off;   // one residual buffer: the alpha candidates run one after the other
+  L.D2 = off;       off = align256(off + sizeof(__half) * N * K);
+  L.total = off;       // two: the next candidate's residual overlaps this one's scoring
   return L;
 }
 
@@ -516,6 +531,21 @@ awq_status_t awq_quantize_pack(const void* W_f16, int64_t N, int64_t K, const fl
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace awq {
+// Smallest workspace awq_search_scale accepts (one residual buffer: candidates in order).
+size_t search_workspace_min_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
+                                  awq_qcfg_t cfg) {
+  if (check_cfg(cfg) != AWQ_OK || check_nk(N, K, cfg) != AWQ_OK || T < 1 || n_alpha < 1 ||
+      n_alpha > 64)
+    return 0;
+  return search_layout(N, K, n_alpha).min_total;
+}
+}  // namespace awq
+
+extern "C" {
+
 size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
                                   awq_qcfg_t cfg) {
   if (check_cfg(cfg) != AWQ_OK || check_nk(N, K, cfg) != AWQ_OK || T < 1 || n_alpha < 1 ||
@@ -539,7 +569,8 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
       (inv_s_out && !aligned16(inv_s_out)) || !aligned16(workspace))
     return AWQ_ERR_MISALIGNED;
   const SearchLayout L = search_layout(N, K, n_alpha);
-  if (!workspace || ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < L.min_total) return AWQ_ERR_WORKSPACE;
+  const bool overlap = ws_bytes >= L.total;
   DeviceInfo* d = nullptr;
   AWQ_TRY(device_info(&d));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -550,13 +581,15 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   float* inv_grid = reinterpret_cast<float*>(ws + L.inv_grid);
   unsigned int* absmax = reinterpret_cast<unsigned int*>(ws + L.absmax);
   double* partial = reinterpret_cast<double*>(ws + L.partial);
-  __half* D = reinterpret_cast<__half*>(ws + L.D);
+  __half* Dbuf[2] = {reinterpret_cast<__half*>(ws + L.D),
+                     reinterpret_cast<__half*>(ws + (overlap ? L.D2 : L.D))};
   const __half* W = static_cast<const __half*>(W_f16);
   const __half* X = static_cast<const __half*>(X_f16);
 
-  CUtensorMap mapX, mapD;
+  CUtensorMap mapX, mapD[2];
   AWQ_TRY(make_map(&mapX, X, T, K, K, score::BM));
-  AWQ_TRY(make_map(&mapD, D, N, K, K, score::BN));
+  AWQ_TRY(make_map(&mapD[0], Dbuf[0], N, K, K, score::BN));
+  AWQ_TRY(make_map(&mapD[1], Dbuf[1], N, K, K, score::BN));
 
   // 1. statistic
   const float* mp = mean_abs;
@@ -599,20 +632,50 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   sp.status = d->status;
   sp.limit_ns = g_wait_limit_ns.load();
   const int sgrid = std::min(sp.num_tiles, std::min(d->sms, kPartialStride));
-  const unsigned rgrid = static_cast<unsigned>((N * (K / 8) + 255) / 256);
-  for (int i = 0; i < n_alpha; ++i) {
+  const dim3 rgrid(static_cast<unsigned>((N + 8 * QROWS - 1) / (8 * QROWS)),
+                   static_cast<unsigned>((K / 8 + 31) / 32));
+  // Residual i goes to buffer i % 2. With two buffers the residual of candidate i + 1 runs on
+  // the side stream while candidate i is scored: the scoring GEMM is tensor-bound and leaves
+  // room on every SM for the memory-bound residual blocks. Events order the two streams (the
+  // side stream forks from and rejoins the caller's stream, so the sequence can be captured in
+  // a graph); with one buffer everything runs in order on the caller's stream.
+  auto residual = [&](int i, cudaStream_t rs) -> awq_status_t {
     ResidualArgs ra{W, s_grid + static_cast<size_t>(i) * K, inv_grid + static_cast<size_t>(i) * K,
-                    absmax, D, static_cast<int>(N), static_cast<int>(K), cfg.symmetric};
-    prof_start(AWQ_K_RESIDUAL, st);
+                    absmax, Dbuf[i & 1], static_cast<int>(N), static_cast<int>(K), cfg.symmetric};
+    prof_start(AWQ_K_RESIDUAL, rs);
     if (cfg.group_size == 128)
-      residual_kernel<128><<<rgrid, 256, 0, st>>>(ra);
+      residual_kernel<128><<<rgrid, 256, 0, rs>>>(ra);
     else
-      residual_kernel<64><<<rgrid, 256, 0, st>>>(ra);
-    AWQ_TRY(launched(AWQ_K_RESIDUAL, st));
+      residual_kernel<64><<<rgrid, 256, 0, rs>>>(ra);
+    return launched(AWQ_K_RESIDUAL, rs);
+  };
+  auto ev = [](cudaError_t e) -> awq_status_t {
+    if (e == cudaSuccess) return AWQ_OK;
+    cudaGetLastError();
+    return AWQ_ERR_CUDA;
+  };
+  cudaStream_t rs = overlap ? d->side : st;
+  if (overlap) {
+    AWQ_TRY(ev(cudaEventRecord(d->fork, st)));
+    AWQ_TRY(ev(cudaStreamWaitEvent(rs, d->fork, 0)));
+  }
+  AWQ_TRY(residual(0, rs));
+  if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[0], rs)));
+  for (int i = 0; i < n_alpha; ++i) {
+    if (overlap) AWQ_TRY(ev(cudaStreamWaitEvent(st, d->res_done[i & 1], 0)));
     sp.partial = partial + static_cast<size_t>(i) * kPartialStride;
     prof_start(AWQ_K_SCORE, st);
-    score::score_kernel<<<sgrid, score::THREADS, score::SMEM_BYTES, st>>>(mapX, mapD, sp);
+    score::score_kernel<<<sgrid, score::THREADS, score::SMEM_BYTES, st>>>(mapX, mapD[i & 1], sp);
     AWQ_TRY(launched(AWQ_K_SCORE, st));
+    if (i + 1 < n_alpha) {
+      if (overlap) {
+        AWQ_TRY(ev(cudaEventRecord(d->score_done[i & 1], st)));
+        // buffer (i + 1) % 2 was last read by the scoring of candidate i - 1
+        if (i >= 1) AWQ_TRY(ev(cudaStreamWaitEvent(rs, d->score_done[(i - 1) & 1], 0)));
+      }
+      AWQ_TRY(residual(i + 1, rs));
+      if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[(i + 1) & 1], rs)));
+    }
   }
   // 5. errors, argmin, winning scales
   prof_start(AWQ_K_FINALIZE, st);

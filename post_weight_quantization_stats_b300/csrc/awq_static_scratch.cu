@@ -15,6 +15,11 @@
 
 #include "../../include/awq.h"
 
+namespace awq {
+size_t search_workspace_min_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
+                                  awq_qcfg_t cfg);
+}
+
 namespace {
 
 static __device__ __align__(256) unsigned char g_search_scratch[AWQ_SEARCH_STATIC_SCRATCH_BYTES];
@@ -53,7 +58,8 @@ extern "C" awq_status_t awq_search_scale_static(const void* W_f16, int64_t N, in
                                                 int32_t n_alpha, awq_qcfg_t cfg, float* err_out,
                                                 int32_t* best_idx, float* s_out,
                                                 float* inv_s_out, awq_stream_t stream) {
-  const size_t need = awq_search_workspace_bytes(N, K, T, n_alpha, cfg);
+  // the smallest workspace the search runs with (one residual buffer, candidates in order)
+  const size_t need = awq::search_workspace_min_bytes(N, K, T, n_alpha, cfg);
   if (need == 0)  // invalid shape or configuration: report the search's own validation error
     return awq_search_scale(W_f16, N, K, X_f16, T, mean_abs, alphas, n_alpha, cfg, nullptr, 0,
                             err_out, best_idx, s_out, inv_s_out, stream);

@@ -8,11 +8,12 @@
 //
 // Every operation that decides a code is an IEEE fp32 operation written as an intrinsic
 // (__fmul_rn, __fsub_rn, __fdiv_rn, rintf), so nothing is contracted into an FMA and the codes
-// are reproducible bit for bit.
+// are reproducible bit for bit; the per-weight division is replaced by a multiplication with
+// the correctly rounded reciprocal wherever that provably gives the same rounded quotient.
 //
-// Thread layout shared by the kernels here: thread i of the grid owns packed word i of the
-// [N, K/8] code matrix, i.e. 8 consecutive input channels of one row; the G/8 threads of a
-// group are consecutive lanes of one warp and reduce the group's min/max with shuffles.
+// Thread layout shared by the quantising kernels here: a lane owns one packed word (8
+// consecutive input channels) of several rows; the G/8 lanes of a group are consecutive lanes
+// of one warp and reduce the group's min/max with shuffles.
 #pragma once
 
 #include "awq_device.cuh"
@@ -22,35 +23,8 @@ namespace awq {
 struct GroupParams {
   float step;  // fp32 step the codes are decided with
   float zero;  // zero point as a float (exact small integer)
+  float rcp;   // 1 / step, correctly rounded
 };
-
-__device__ __forceinline__ void load_scaled8(const __half* __restrict__ w_row8,
-                                             const float* __restrict__ s8, bool valid,
-                                             float (&wp)[8], float (&w)[8]) {
-  if (!valid) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { wp[i] = 0.f; w[i] = 0.f; }
-    return;
-  }
-  const uint4 raw = *reinterpret_cast<const uint4*>(w_row8);
-  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(h2[i]);
-    w[2 * i] = f.x;
-    w[2 * i + 1] = f.y;
-  }
-  if (s8 != nullptr) {
-    const float4 sa = __ldg(reinterpret_cast<const float4*>(s8));
-    const float4 sb = __ldg(reinterpret_cast<const float4*>(s8) + 1);
-    const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) wp[i] = __fmul_rn(w[i], sv[i]);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) wp[i] = w[i];
-  }
-}
 
 // Group step and zero point; TEAM = G / 8 consecutive lanes hold one group.
 template <int TEAM>
@@ -74,6 +48,7 @@ __device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool s
     if (st == 0.0f) st = 1.0f;
     g.step = st;
     g.zero = 8.0f;
+    g.rcp = __frcp_rn(st);
   } else {
     hi = fmaxf(hi, 0.0f);
     lo = fminf(lo, 0.0f);
@@ -83,13 +58,26 @@ __device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool s
     z = fminf(fmaxf(z, 0.0f), 15.0f);
     g.step = st;
     g.zero = z;
+    g.rcp = __frcp_rn(st);
   }
   return g;
 }
 
+// rint(fl32(wp / step)) without a division in the common case. |wp / step| <= 15 for every
+// weight of the group, so t = fl32(wp * fl32(1 / step)) is within 2^-19 of the exact quotient
+// and fl32 of the quotient within 2^-20 of it: unless t lies within 2^-17 of a half-integer (a
+// rounding boundary of rint), t and the IEEE quotient round to the same integer. Near a
+// boundary (about 1.5e-5 of all weights) the quotient is computed with IEEE division.
+__device__ __forceinline__ float rint_quotient(float wp, const GroupParams& g) {
+  const float t = __fmul_rn(wp, g.rcp);
+  const float f = __fsub_rn(t, floorf(t));
+  if (fabsf(__fsub_rn(f, 0.5f)) <= 0x1p-17f) return rintf(__fdiv_rn(wp, g.step));
+  return rintf(t);
+}
+
 // Stored code (0..15) of one scaled weight.
 __device__ __forceinline__ uint32_t code_of(float wp, const GroupParams& g, bool symmetric) {
-  float r = rintf(__fdiv_rn(wp, g.step));
+  float r = rint_quotient(wp, g);
   if (symmetric) {
     r = fminf(fmaxf(r, -8.0f), 7.0f) + 8.0f;
   } else {
@@ -109,30 +97,74 @@ struct QuantArgs {
   int N, K, symmetric;
 };
 
+// Row-tiled launch shape shared by quantize_pack_kernel and residual_kernel: a block of 8 warps
+// covers 32 packed words (256 channels) of 8 * QROWS rows (rows along grid x, 256-channel column
+// chunks along grid y); lane l owns word 32 blockIdx.y + l of the QROWS rows of its warp. The per-channel scales are loaded once per lane and the QROWS
+// 16-byte weight loads are issued together, so every thread keeps 64 bytes of HBM reads in
+// flight. A group (G / 8 words) is G / 8 consecutive lanes of one row.
+constexpr int QROWS = 4;
+
+__device__ __forceinline__ void load8f(const float* p, bool ok, float fill, float (&v)[8]) {
+  if (ok) {
+    const float4 lo = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 hi = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+    v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = fill;
+  }
+}
+
+__device__ __forceinline__ void unpack8(const uint4& raw, float (&w)[8]) {
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h2[i]);
+    w[2 * i] = f.x;
+    w[2 * i + 1] = f.y;
+  }
+}
+
 template <int G>
 __global__ void __launch_bounds__(256) quantize_pack_kernel(QuantArgs a) {
   constexpr int TEAM = G / 8;
   const int kw = a.K >> 3;                                   // words per row
-  const long long total = static_cast<long long>(a.N) * kw;
-  const long long word = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool valid = word < total;
-  const int n = valid ? static_cast<int>(word / kw) : 0;
-  const int w = valid ? static_cast<int>(word - static_cast<long long>(n) * kw) : 0;
-  const int k0 = w * 8;
-  float wp[8], wv[8];
-  load_scaled8(a.W + static_cast<long long>(n) * a.K + k0, a.s ? a.s + k0 : nullptr, valid, wp,
-               wv);
-  const bool sym = a.symmetric != 0;
-  const GroupParams g = group_params<TEAM>(wp, sym);
-  if (!valid) return;
-  uint32_t packed = 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.y * 32 + lane;
+  const bool wok = w < kw;
+  const int k0 = (wok ? w : 0) * 8;
+  const int rbase = (blockIdx.x * 8 + warp) * QROWS;
+  float sv[8];
+  load8f(a.s + k0, wok && a.s != nullptr, 1.0f, sv);
+  uint4 raw[QROWS];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) packed |= code_of(wp[i], g, sym) << (4 * i);
-  a.qweight[word] = packed;
-  if ((threadIdx.x & (TEAM - 1)) == 0) {
-    const long long gi = static_cast<long long>(k0 / G) * a.N + n;
-    a.scales[gi] = __float2half_rn(g.step);
-    if (!sym && a.zeros) a.zeros[gi] = static_cast<uint8_t>(g.zero);
+  for (int r = 0; r < QROWS; ++r) {
+    const int row = rbase + r;
+    raw[r] = (wok && row < a.N)
+                 ? __ldg(reinterpret_cast<const uint4*>(a.W + static_cast<long long>(row) * a.K + k0))
+                 : make_uint4(0, 0, 0, 0);
+  }
+  const bool sym = a.symmetric != 0;
+#pragma unroll
+  for (int r = 0; r < QROWS; ++r) {
+    const int row = rbase + r;
+    float wv[8], wp[8];
+    unpack8(raw[r], wv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wp[i] = a.s ? __fmul_rn(wv[i], sv[i]) : wv[i];
+    const GroupParams g = group_params<TEAM>(wp, sym);   // every lane takes part in the shuffles
+    if (wok && row < a.N) {
+      uint32_t packed = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) packed |= code_of(wp[i], g, sym) << (4 * i);
+      a.qweight[static_cast<long long>(row) * kw + w] = packed;
+      if ((lane & (TEAM - 1)) == 0) {
+        const long long gi = static_cast<long long>(k0 / G) * a.N + row;
+        a.scales[gi] = __float2half_rn(g.step);
+        if (!sym && a.zeros) a.zeros[gi] = static_cast<uint8_t>(g.zero);
+      }
+    }
   }
 }
 
@@ -207,31 +239,45 @@ template <int G>
 __global__ void __launch_bounds__(256) residual_kernel(ResidualArgs a) {
   constexpr int TEAM = G / 8;
   const int kw = a.K >> 3;
-  const long long total = static_cast<long long>(a.N) * kw;
-  const long long word = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool valid = word < total;
-  const int n = valid ? static_cast<int>(word / kw) : 0;
-  const int w = valid ? static_cast<int>(word - static_cast<long long>(n) * kw) : 0;
-  const int k0 = w * 8;
-  float wp[8], wv[8];
-  load_scaled8(a.W + static_cast<long long>(n) * a.K + k0, a.s + k0, valid, wp, wv);
-  const bool sym = a.symmetric != 0;
-  const GroupParams g = group_params<TEAM>(wp, sym);
-  if (!valid) return;
-  const float step16 = __half2float(__float2half_rn(g.step));
-  const float p2 = ldexpf(1.0f, residual_exponent(*a.absmax));
-  const float4 ia = __ldg(reinterpret_cast<const float4*>(a.inv_s + k0));
-  const float4 ib = __ldg(reinterpret_cast<const float4*>(a.inv_s + k0) + 1);
-  const float inv[8] = {ia.x, ia.y, ia.z, ia.w, ib.x, ib.y, ib.z, ib.w};
-  __align__(16) __half out[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.y * 32 + lane;
+  const bool wok = w < kw;
+  const int k0 = (wok ? w : 0) * 8;
+  const int rbase = (blockIdx.x * 8 + warp) * QROWS;
+  float sv[8], iv[8];
+  load8f(a.s + k0, wok, 1.0f, sv);
+  load8f(a.inv_s + k0, wok, 1.0f, iv);
+  uint4 raw[QROWS];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float qz = static_cast<float>(code_of(wp[i], g, sym)) - g.zero;  // exact
-    const float w_hat = __fmul_rn(__fmul_rn(qz, step16), inv[i]);
-    out[i] = __float2half_rn(__fmul_rn(__fsub_rn(wv[i], w_hat), p2));
+  for (int r = 0; r < QROWS; ++r) {
+    const int row = rbase + r;
+    raw[r] = (wok && row < a.N)
+                 ? __ldg(reinterpret_cast<const uint4*>(a.W + static_cast<long long>(row) * a.K + k0))
+                 : make_uint4(0, 0, 0, 0);
   }
-  *reinterpret_cast<uint4*>(a.D + static_cast<long long>(n) * a.K + k0) =
-      *reinterpret_cast<const uint4*>(out);
+  const bool sym = a.symmetric != 0;
+  const float p2 = ldexpf(1.0f, residual_exponent(*a.absmax));
+#pragma unroll
+  for (int r = 0; r < QROWS; ++r) {
+    const int row = rbase + r;
+    float wv[8], wp[8];
+    unpack8(raw[r], wv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wp[i] = __fmul_rn(wv[i], sv[i]);
+    const GroupParams g = group_params<TEAM>(wp, sym);   // every lane takes part in the shuffles
+    if (wok && row < a.N) {
+      const float step16 = __half2float(__float2half_rn(g.step));
+      __align__(16) __half out[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float qz = static_cast<float>(code_of(wp[i], g, sym)) - g.zero;  // exact
+        const float w_hat = __fmul_rn(__fmul_rn(qz, step16), iv[i]);
+        out[i] = __float2half_rn(__fmul_rn(__fsub_rn(wv[i], w_hat), p2));
+      }
+      *reinterpret_cast<uint4*>(a.D + static_cast<long long>(row) * a.K + k0) =
+          *reinterpret_cast<const uint4*>(out);
+    }
+  }
 }
 
 }  // namespace awq

@@ -7,7 +7,10 @@
 // D[n, t] = sum_k A[n, k] B[t, k].
 //
 // Two kernels share the pipeline skeleton (TMA producer warp, one MMA-issuing thread, four
-// epilogue warps that own the 128 TMEM lanes, eight expander warps):
+// epilogue warps that own the 128 TMEM lanes, eight expander warps that build the A operand).
+// The A operand lives in tensor memory: the expanders write it with tcgen05.st (each warp into
+// the 32-lane quarter it may access) and tcgen05.mma reads it from there, so shared memory
+// carries only the TMA traffic (codes, activations, inv_s) and the small B tile.
 //
 // grouped_kernel (M <= 16 tokens: decode and small batches; HBM-bound)
 //   Moves the group scaling out of the per-weight work. A is the raw nibble expansion: a code q
@@ -22,18 +25,19 @@
 //   warp shuffle. A tile therefore carries 120 weight rows. Each group accumulates into its own
 //   TMEM slot and the epilogue adds
 //       y[t, n] += step[n, g] * (D_g[n, t] - C[g, t] - z[n, g] S[g, t]),
-//   so the expanders spend no FMA-pipe instruction per weight. Stages are 64 channels, two
-//   CTAs share an SM, and K is split across a cluster of CTAs whose partial sums are added
-//   in rank order through distributed shared memory (deterministic, no global scratch).
+//   so the expanders spend no FMA-pipe instruction per weight. TMA brings 256 channels of codes
+//   per stage (128 bytes per row, the width at which the box stream reaches HBM speed), the MMA
+//   consumes them in 64-channel steps, two CTAs share an SM, and K is split across a cluster of
+//   CTAs whose partial sums are added in rank order through distributed shared memory
+//   (deterministic, no global scratch).
 //
 // dequant_kernel (M > 16: prefill batches; tensor-bound)
-//   A is the fp16 weight (q - z) * step (* inv_s) in natural channel order, written by the
-//   expanders into the 128B-swizzled K-major tile; X arrives by TMA in the same swizzle. One
-//   128 x BN accumulator per CTA; K split across a cluster as above when the tiles alone do
-//   not fill the GPU.
+//   A is the fp16 weight (q - z) * step (* inv_s) in natural channel order; X arrives by TMA in
+//   the 128B-swizzled K-major layout. One 128 x BN accumulator per CTA; K split across a
+//   cluster as above when the tiles alone do not fill the GPU.
 //
-// The codes of every stage arrive by TMA (a [N, K/8] uint32 tensor map, 128-row boxes), so
-// the ring keeps several stages of weight reads in flight. Every wait is bounded.
+// The codes of every stage arrive by TMA (a [N, K/8] uint32 tensor map), so the ring keeps
+// several stages of weight reads in flight. Every wait is bounded.
 #pragma once
 
 #include <cooperative_groups.h>

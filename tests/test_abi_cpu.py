@@ -38,8 +38,8 @@ def test_status_strings(L):
 
 def test_workspace_bytes(L):
     n = awq.awq_search_workspace_bytes(4096, 4096, 8192, 20)
-    assert n >= 4096 * 4096 * 2          # the fp16 residual of one candidate
-    assert n < 4096 * 4096 * 2 + (4 << 20)
+    assert n >= 2 * 4096 * 4096 * 2      # two fp16 residual buffers (overlapped schedule)
+    assert n < 2 * 4096 * 4096 * 2 + (4 << 20)
     assert awq.awq_search_workspace_bytes(4096, 4100, 8192, 20) == 0   # K % G
     assert awq.awq_search_workspace_bytes(4096, 4096, 8192, 65) == 0   # too many alphas
     assert awq.awq_search_workspace_bytes(4096, 4096, 8192, 20, group_size=96) == 0
@@ -73,7 +73,10 @@ def test_host_validation_rejects_without_cuda(L):
     alphas = (ctypes.c_float * 2)(0.0, 0.5)
     ap = ctypes.cast(alphas, ctypes.c_void_p)
     ws = awq.awq_search_workspace_bytes(16, 256, 8, 2)
-    assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, ap, 2, cfg, A, ws - 1, A, A,
+    ws_min = ws - (16 * 256 * 2 + 255) // 256 * 256    # one residual buffer instead of two
+    assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, ap, 2, cfg, A, ws_min, A, A,
+                 None, None, None) == S["AWQ_ERR_NO_DEVICE"]    # accepted: only the device check fails
+    assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, ap, 2, cfg, A, ws_min - 1, A, A,
                  None, None, None) == S["AWQ_ERR_WORKSPACE"]
     assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, ap, 0, cfg, A, ws, A, A,
                  None, None, None) == S["AWQ_ERR_INVALID_ARG"]

@@ -200,6 +200,23 @@ def test_search_deterministic():
         assert torch.equal(u, v)
 
 
+def test_search_overlapped_schedule_matches_serial():
+    """Two residual buffers (next candidate's residual built on a second stream while the
+    current one is scored) and one buffer (candidates in order) give bit-identical results."""
+    d = layer(12, 700, 1536, 333, n_out=6)
+    W, X = dev(d["W"]), dev(d["X"])
+    N, K = W.shape
+    alphas = synth.alpha_grid(20)
+    full = awq.awq_search_workspace_bytes(N, K, X.shape[0], 20)
+    one = full - (N * K * 2 + 255) // 256 * 256
+    a = awq.search_scale(W, X, alphas)
+    b = awq.search_scale(W, X, alphas,
+                         workspace=torch.empty(one, dtype=torch.uint8, device="cuda"))
+    awq.awq_stream_status()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
 @pytest.mark.slow
 def test_search_full_size_llama7b_attn():
     """K = N = 4096, T = 8192 (the benchmark's layer), in the benchmark's launch configuration:
