@@ -351,7 +351,9 @@ awq_status_t gemv_shape(gemv::Args& a, int G, int sms) {
   a.rows_stage = std::max(a.row_groups, (32768 / row_bytes) / a.row_groups * a.row_groups);
   a.stage_bytes = a.rows_stage * row_bytes;
   a.pstride = a.K / G + 1;
-  a.nstages = gemv::MAX_STAGES;
+  // no more stages than the CTA's rows fill (at least 2)
+  const int stages_needed = (a.rows_max + a.rows_stage - 1) / a.rows_stage;
+  a.nstages = std::max(2, std::min(gemv::MAX_STAGES, stages_needed));
   while (a.nstages > 2 && gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) --a.nstages;
   if (gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) return AWQ_ERR_UNSUPPORTED_SHAPE;
   return AWQ_OK;
@@ -367,9 +369,20 @@ awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
     return AWQ_ERR_CUDA;
   }
   const unsigned grid = static_cast<unsigned>((a.N + a.rows_max - 1) / a.rows_max);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(gemv::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see the kernel's header
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_start(AWQ_K_GEMV, st);
-  kern<<<grid, gemv::THREADS, smem, st>>>(a);
-  return launched(AWQ_K_GEMV, st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  const awq_status_t rl = launched(AWQ_K_GEMV, st);
+  return e != cudaSuccess ? AWQ_ERR_CUDA : rl;
 }
 
 // Sum of the per-CTA partials of every alpha in fixed order, the 2^-2p of the residual scale

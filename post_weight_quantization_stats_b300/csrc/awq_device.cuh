@@ -99,6 +99,18 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
+// ------------------------------------------------------------------------------ PDL
+
+// Programmatic dependent launch: lets the next kernel of the stream (launched with programmatic
+// stream serialization) start once every CTA of this grid has issued this or exited.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their writes are visible
+// (returns at once when there are none).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------ TMA
 
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes on `bar`.

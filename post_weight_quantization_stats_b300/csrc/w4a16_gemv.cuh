@@ -11,9 +11,10 @@
 // evict-first): every CTA keeps 100+ KB of weight reads in flight without spending registers.
 //
 // The consumers are P x RG warps: part p of K (IPL items of 32 channels per lane, 1024 * IPL
-// channels per warp) times row group rg. A lane's activations never change, so each warp
-// loads its K slice of x~ = x * inv_s once, into registers, at the start; the only
-// shared-memory traffic per code is the bulk copy's write and one 16-byte read per item. Per
+// channels per warp) times row group rg. A lane's activations never change: the CTA stages
+// x~ = x * inv_s once in shared memory with coalesced loads, and each lane copies its K slice
+// into registers; afterwards the only shared-memory traffic per code is the bulk copy's write
+// and one 16-byte read per item. Per
 // item and row:
 //   * codes become exact (q - z) half2 pairs by the 0x6400 fp16 exponent trick (q + 1024 sits
 //     in the mantissa of a half in [1024, 2048));
@@ -23,6 +24,12 @@
 //   * the item sum is scaled by 64 * step and accumulated in fp32.
 // Row partials are reduced with shuffles and written to shared memory per (row, part); the
 // parts are added in a fixed order at the end, so the result is deterministic.
+//
+// Launched with programmatic dependent launch: the kernel lets the next W4A16 launch of the
+// stream start right after its own set-up, and it streams its weights and stages its group
+// parameters before waiting (griddepcontrol.wait) for the previous kernel, so back-to-back
+// decode layers overlap one layer's weight prefetch with the previous layer's tail. The ring
+// has only as many stages as the CTA's rows need, which keeps the next kernel's CTAs resident.
 #pragma once
 
 #include "awq_device.cuh"
@@ -66,9 +73,13 @@ __host__ __device__ inline int ysum_floats(const Args& a) {
   return (a.rows_max * a.parts * a.M + 3) & ~3;
 }
 __host__ __device__ inline int param_words(const Args& a) { return (a.rows_max * a.pstride + 3) & ~3; }
+__host__ __device__ inline size_t xs_bytes(const Args& a) {
+  return static_cast<size_t>(a.M) * static_cast<size_t>(a.K) * 2;
+}
 __host__ __device__ inline size_t smem_bytes(const Args& a) {
-  return static_cast<size_t>(a.nstages) * a.stage_bytes + static_cast<size_t>(param_words(a)) * 4 +
-         static_cast<size_t>(ysum_floats(a)) * 4 + 2 * MAX_STAGES * 8 + 16;
+  return static_cast<size_t>(a.nstages) * a.stage_bytes + xs_bytes(a) +
+         static_cast<size_t>(param_words(a)) * 4 + static_cast<size_t>(ysum_floats(a)) * 4 +
+         2 * MAX_STAGES * 8 + 16;
 }
 
 // 8 codes of one word -> 4 exact half2 (q - z) pairs in the order (0,4), (1,5), (2,6), (3,7).
@@ -103,18 +114,21 @@ __device__ __forceinline__ void stage_params(const Args& a, uint32_t* prm, int r
   }
 }
 
-// x~ / 64 of one item (channels 32 it .. 32 it + 31) of token m, in the unpacking's pair order.
-__device__ __forceinline__ void load_x_item(const Args& a, int m, int it, __half2 (&xr)[16]) {
-  const int k = it * ITEM_CH;
-  const uint4* xp = reinterpret_cast<const uint4*>(a.X + static_cast<long long>(m) * a.K + k);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 raw = __ldg(xp + v);
+// x~ / 64 of every token, staged once per CTA with coalesced 16-byte loads: slot j (channels
+// 8j .. 8j+7) of token m holds the pair order (x0,x4), (x1,x5), (x2,x6), (x3,x7). fp16(x * inv_s)
+// is what the folded activation would be; the 2^-6 prescale is exact on it.
+template <int M>
+__device__ __forceinline__ void stage_x(const Args& a, uint4* xs) {
+  const int slots = a.K / 8;
+  for (int idx = threadIdx.x; idx < M * slots; idx += CTHREADS) {
+    const int m = idx / slots, j = idx - (idx / slots) * slots;
+    const int k = 8 * j;
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.X + static_cast<long long>(m) * a.K + k));
     const __half* xv = reinterpret_cast<const __half*>(&raw);
     float f[8];
     if (a.inv_s) {
-      const float4 ia = __ldg(reinterpret_cast<const float4*>(a.inv_s + k + 8 * v));
-      const float4 ib = __ldg(reinterpret_cast<const float4*>(a.inv_s + k + 8 * v) + 1);
+      const float4 ia = __ldg(reinterpret_cast<const float4*>(a.inv_s + k));
+      const float4 ib = __ldg(reinterpret_cast<const float4*>(a.inv_s + k) + 1);
       const float iv[8] = {ia.x, ia.y, ia.z, ia.w, ib.x, ib.y, ib.z, ib.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = __half2float(xv[e]) * iv[e];
@@ -122,11 +136,12 @@ __device__ __forceinline__ void load_x_item(const Args& a, int m, int it, __half
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = __half2float(xv[e]);
     }
-    // fp16(x * inv_s) is what the folded activation would be; the 2^-6 prescale is exact on it
+    __align__(16) __half2 pr[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      xr[v * 4 + e] = __halves2half2(__float2half_rn(__half2float(__float2half_rn(f[e])) * X_PRESCALE),
-                                     __float2half_rn(__half2float(__float2half_rn(f[e + 4])) * X_PRESCALE));
+      pr[e] = __halves2half2(__float2half_rn(__half2float(__float2half_rn(f[e])) * X_PRESCALE),
+                             __float2half_rn(__half2float(__float2half_rn(f[e + 4])) * X_PRESCALE));
+    xs[idx] = *reinterpret_cast<const uint4*>(pr);
   }
 }
 
@@ -135,7 +150,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
   constexpr int IPL = items_per_lane(M);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  uint32_t* prm = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(a.nstages) * a.stage_bytes);
+  uint4* xs = reinterpret_cast<uint4*>(smem + static_cast<size_t>(a.nstages) * a.stage_bytes);
+  uint32_t* prm = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(xs) + xs_bytes(a));
   float* ysum = reinterpret_cast<float*>(prm + param_words(a));
   uint64_t* full = reinterpret_cast<uint64_t*>(ysum + ysum_floats(a));
   uint64_t* empty = full + MAX_STAGES;
@@ -158,6 +174,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
   }
   __syncthreads();
   const WaitCtx wc{a.limit_ns, abort_flag, a.status};
+  // The next W4A16 launch of the stream may start now: it only prefetches its own weights and
+  // group parameters until its griddepcontrol.wait.
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == CWARPS) {
     // ------------------------------------------------------------ producer: code stream
@@ -187,6 +206,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
   const bool active = warp < a.parts * a.row_groups;
   const int part = warp % a.parts, rg = warp / a.parts;
   const int items = a.K / ITEM_CH;
+  stage_params<G>(a, prm, r0, nrows);
+  // Activations (and the output) may belong to the previous kernel of the stream: everything
+  // below waits for it. The weight stream and the group parameters above do not.
+  pdl_wait();
+  stage_x<M>(a, xs);
+  named_bar_sync(1, CTHREADS);
+  // each lane's x~ slice: 4 consecutive 16-byte slots per item (conflict-free: a warp reads
+  // 32 consecutive items' slots in four passes)
   __half2 xr[M][IPL][16];
   if (active) {
 #pragma unroll
@@ -194,17 +221,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
       const int it = part * IPL * 32 + lane + 32 * u;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        if (it < items) {
-          load_x_item(a, m, it, xr[m][u]);
-        } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) xr[m][u][e] = __float2half2_rn(0.f);
+        for (int v = 0; v < 4; ++v) {
+          const uint4 q = it < items ? xs[m * (a.K / 8) + it * 4 + v] : make_uint4(0, 0, 0, 0);
+          const __half2* h2 = reinterpret_cast<const __half2*>(&q);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) xr[m][u][v * 4 + e] = h2[e];
         }
       }
     }
   }
-  stage_params<G>(a, prm, r0, nrows);
-  named_bar_sync(1, CTHREADS);
 
   const __half2 c960 = __float2half2_rn(960.0f);
   bool ok = true;
