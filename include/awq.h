@@ -83,11 +83,33 @@ awq_status_t awq_calib_stats(const void* X_f16, int64_t T, int64_t K, int64_t ld
                              float* mean_abs, awq_stream_t stream);
 
 /*
- * Bytes of device workspace for awq_search_scale's fastest schedule (0 on invalid input): two
- * residual buffers, so the next alpha candidate's residual is built while the current one is
- * scored. awq_search_scale also accepts less, down to one residual buffer (this value minus
- * 2 N K bytes rounded up to 256), and then scores the candidates strictly one after the other
- * (same results, bit for bit).
+ * How awq_search_scale computes E(alpha) (process-wide setting, default AWQ_SCORE_AUTO):
+ *   DIRECT  sum of squares of X D^T per candidate (D = W - w_hat): 2 T N K flops each.
+ *   GRAM    E = 1/(T N) sum_n d_n^T H d_n with H = X^T X formed once per call (about T K^2
+ *           flops) and stored as fp16 after a power-of-two scale; each candidate then takes
+ *           about 2 N K^2 / 2 flops over the lower triangle of H. Equal to DIRECT in exact
+ *           arithmetic, so the errors agree to rounding (fp16 H: relative 2^-11 per entry).
+ *   AUTO    GRAM when it takes fewer tensor-core steps (long calibration sets, T > K / 2 or
+ *           so), the workspace holds it, and K T, K K < 2^31; DIRECT otherwise.
+ * Returns AWQ_ERR_INVALID_ARG for any other value.
+ */
+typedef enum { AWQ_SCORE_AUTO = 0, AWQ_SCORE_DIRECT = 1, AWQ_SCORE_GRAM = 2 } awq_score_mode_t;
+awq_status_t awq_set_score_mode(awq_score_mode_t mode);
+
+/*
+ * Bytes of device workspace for awq_search_scale's fastest schedule under the current score
+ * mode (0 on invalid input). Schedules, from the most workspace to the least:
+ *   GRAM     two residual buffers plus X^T ([K, Tp] fp16, Tp = T rounded up to 64), the fp16
+ *            triangle of H ([K, K]) and K Tp / 16 bytes of column sums: returned when the
+ *            mode is GRAM, or AUTO and GRAM pays for this shape.
+ *   OVERLAP  two residual buffers, so the next candidate's residual is built while the
+ *            current one is scored (DIRECT scoring).
+ *   SERIAL   one residual buffer (the OVERLAP size minus 2 N K bytes rounded up to 256): the
+ *            candidates run strictly one after the other, with the same results as OVERLAP,
+ *            bit for bit.
+ * awq_search_scale takes the first schedule the given workspace holds (in AUTO, GRAM only
+ * where it pays). Every schedule is deterministic; GRAM and the DIRECT schedules agree to
+ * rounding, not bit for bit.
  */
 size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
                                   awq_qcfg_t cfg);
@@ -191,12 +213,15 @@ typedef enum {
   AWQ_K_SCALE_GRID = 1,  /* search: s and 1/s for every alpha */
   AWQ_K_ABSMAX = 2,      /* search: max|W| for the residual's power-of-two scale */
   AWQ_K_RESIDUAL = 3,    /* search: W - Q(W diag s) diag(s)^-1 of one alpha, fp16 */
-  AWQ_K_SCORE = 4,       /* search: tcgen05 sum of squares of X D^T of one alpha */
+  AWQ_K_SCORE = 4,       /* search, DIRECT: tcgen05 sum of squares of X D^T of one alpha */
   AWQ_K_FINALIZE = 5,    /* search: errors, argmin, winning scales */
   AWQ_K_QUANTIZE_PACK = 6,
-  AWQ_K_GEMV = 7,        /* awq_w4a16_gemm, M <= 8 */
-  AWQ_K_GEMM_TC = 8,     /* awq_w4a16_gemm, M > 8 */
-  AWQ_K_COUNT = 9
+  AWQ_K_GEMV = 7,        /* awq_w4a16_gemm, CUDA-core kernel for M <= 2 */
+  AWQ_K_GEMM_TC = 8,     /* awq_w4a16_gemm, tcgen05 kernels for larger M */
+  AWQ_K_GRAM_PREP = 9,   /* search, GRAM: X^T, column sums of squares and their maximum */
+  AWQ_K_GRAM = 10,       /* search, GRAM: tcgen05 lower triangle of H = X^T X, fp16 */
+  AWQ_K_SCORE_GRAM = 11, /* search, GRAM: tcgen05 sum_n d_n^T H d_n of one alpha */
+  AWQ_K_COUNT = 12
 } awq_kernel_id_t;
 
 /*

@@ -58,12 +58,14 @@ _SIGNATURES = {
     "awq_stream_status": (ctypes.c_int, [_c_void_p]),
     "awq_launch_count": (ctypes.c_uint64, []),
     "awq_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "awq_set_score_mode": (ctypes.c_int, [ctypes.c_int]),
     "awq_profile_begin": (ctypes.c_int, []),
     "awq_profile_end": (ctypes.c_int, [_c_void_p, _c_void_p]),
 }
 
 KERNELS = ("calib_stats", "scale_grid", "absmax", "residual", "score", "finalize",
-           "quantize_pack", "gemv", "gemm_tc")
+           "quantize_pack", "gemv", "gemm_tc", "gram_prep", "gram", "score_gram")
+SCORE_MODES = {"auto": 0, "direct": 1, "gram": 2}
 
 _lib = None
 
@@ -177,6 +179,11 @@ def awq_launch_count() -> int:
 
 def awq_set_wait_limit_ns(limit_ns: int) -> int:
     return int(lib().awq_set_wait_limit_ns(int(limit_ns)))
+
+
+def awq_set_score_mode(mode):
+    """Process-wide choice of how the search scores candidates: "auto", "direct" or "gram"."""
+    _check("awq_set_score_mode", lib().awq_set_score_mode(SCORE_MODES.get(mode, mode)))
 
 
 def awq_profile_begin():

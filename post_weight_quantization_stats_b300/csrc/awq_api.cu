@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -17,6 +18,7 @@
 #include "../../include/awq.h"
 #include "awq_device.cuh"
 #include "calib_stats.cuh"
+#include "gram_score.cuh"
 #include "quant.cuh"
 #include "score_gemm.cuh"
 #include "w4a16_gemm_tc.cuh"
@@ -30,6 +32,7 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_score_mode{AWQ_SCORE_AUTO};
 constexpr int kMaxDevices = 64;
 constexpr int kPartialStride = 1024;  // per-alpha slots for per-CTA partial sums
 
@@ -387,8 +390,11 @@ awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
 
 // Sum of the per-CTA partials of every alpha in fixed order, the 2^-2p of the residual scale
 // and the 1/(T N) of the mean; first minimiser in fp64; copy out s and 1/s of the winner.
+// With the Gram schedule (hmax != NULL) the partials hold 2^-h sum_n d^T H' d, i.e. half of
+// 2^-h sum_n d^T H d: the factor 2^(1 + h) restores it.
 __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, int nparts,
                                                        int n_alpha, const unsigned int* absmax,
+                                                       const unsigned int* hmax,
                                                        double tn, const float* s_grid,
                                                        const float* inv_grid, int K,
                                                        float* err_out, int* best_idx,
@@ -399,7 +405,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, in
   if (threadIdx.x < static_cast<unsigned>(n_alpha)) {
     double sum = 0.0;
     for (int c = 0; c < nparts; ++c) sum += partial[threadIdx.x * kPartialStride + c];
-    const double v = ldexp(sum, -2 * p2) / tn;
+    const int h = hmax ? 1 + gram::gram_exponent(*hmax) : 0;
+    const double v = ldexp(sum, h - 2 * p2) / tn;
     e[threadIdx.x] = v;
     err_out[threadIdx.x] = static_cast<float>(v);
   }
@@ -422,11 +429,13 @@ __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, in
 
 struct SearchLayout {
   size_t m, s_grid, inv_grid, absmax, partial, D, D2, min_total, total;
+  size_t hmax, colsq, xt, bmat, gram_total;   // Gram schedule: H from X^T, its scaled triangle
+  int64_t Tp;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-SearchLayout search_layout(int64_t N, int64_t K, int32_t n_alpha) {
+SearchLayout search_layout(int64_t N, int64_t K, int64_t T, int32_t n_alpha) {
   SearchLayout L{};
   size_t off = 0;
   L.m = off;        off = align256(off + sizeof(float) * K);
@@ -438,7 +447,71 @@ SearchLayout search_layout(int64_t N, int64_t K, int32_t n_alpha) {
   L.min_total = off;   // one residual buffer: the alpha candidates run one after the other
   L.D2 = off;       off = align256(off + sizeof(__half) * N * K);
   L.total = off;       // two: the next candidate's residual overlaps this one's scoring
+  L.Tp = (T + gram::TOK_BLOCK - 1) / gram::TOK_BLOCK * gram::TOK_BLOCK;
+  L.hmax = off;     off = align256(off + sizeof(unsigned int));
+  L.colsq = off;    off = align256(off + sizeof(float) * (L.Tp / gram::TOK_BLOCK) * K);
+  L.xt = off;       off = align256(off + sizeof(__half) * K * L.Tp);
+  L.bmat = off;     off = align256(off + sizeof(__half) * K * K);
+  L.gram_total = off;  // Gram schedule (two residual buffers as well)
   return L;
+}
+
+// Shapes the Gram schedule handles: 32-bit element offsets for X^T and H, a transpose grid
+// within the launch limits.
+bool gram_shape_ok(int64_t K, int64_t T) {
+  const int64_t Tp = (T + gram::TOK_BLOCK - 1) / gram::TOK_BLOCK * gram::TOK_BLOCK;
+  return K * Tp <= kMaxElems && K * K <= kMaxElems && Tp / gram::TOK_BLOCK <= 65535;
+}
+
+// Tile counts of the Gram schedule's two kernel modes.
+int gram_tiles(int64_t K) {  // GRAM mode: row tiles kt = 0..KT-1 take kt / 2 + 1 tiles each
+  const int KT = static_cast<int>((K + gram::BM - 1) / gram::BM);
+  int n = 0;
+  for (int kt = 0; kt < KT; ++kt) n += kt / 2 + 1;
+  return n;
+}
+
+// Whether scoring through H = X^T X takes fewer tensor-core tile steps (one 128 x 256 x 64
+// MMA block each, counted on the most loaded of `sms` CTAs) than the direct X D^T, including
+// forming H once and the transpose of X (converted at about 1.5 MB of traffic per step).
+bool gram_pays(int64_t N, int64_t K, int64_t T, int32_t n_alpha, int sms) {
+  const int64_t P = sms;
+  const int64_t direct_tiles = ((T + 127) / 128) * ((N + 255) / 256);
+  const double direct = static_cast<double>((direct_tiles + P - 1) / P) * ((K + 63) / 64);
+  const int64_t RT = (N + gram::BM - 1) / gram::BM, CT = (K + gram::BN - 1) / gram::BN;
+  std::vector<int64_t> load(static_cast<size_t>(P), 0);
+  for (int64_t u = 0; u < RT * CT; ++u) {  // the kernel's serpentine deal, longest tiles first
+    const int64_t ct = CT - 1 - u / RT, r = u / P, pos = u % P;
+    const int64_t cta = (r & 1) ? P - 1 - pos : pos;
+    load[static_cast<size_t>(cta)] += (std::min<int64_t>((ct + 1) * gram::BN, K) + 63) / 64;
+  }
+  int64_t per_alpha = 0;
+  for (int64_t v : load) per_alpha = std::max(per_alpha, v);
+  const int64_t Tp = (T + 63) / 64 * 64;
+  const double once = static_cast<double>((gram_tiles(K) + P - 1) / P) * (Tp / 64) +
+                      4.0 * static_cast<double>(T) * static_cast<double>(K) / 1.5e6;
+  return static_cast<double>(n_alpha) * per_alpha + once < static_cast<double>(n_alpha) * direct;
+}
+
+// The schedule a search with `ws_bytes` of workspace takes (ws_bytes = SIZE_MAX: the one the
+// library prefers). Returns false if the workspace is too small.
+enum class Sched { SERIAL, OVERLAP, GRAM };
+bool pick_schedule(int64_t N, int64_t K, int64_t T, int32_t n_alpha, size_t ws_bytes, int sms,
+                   const SearchLayout& L, Sched* out) {
+  const int mode = g_score_mode.load();
+  const bool gram_ok = gram_shape_ok(K, T);
+  const bool want_gram = gram_ok && (mode == AWQ_SCORE_GRAM ||
+                                     (mode == AWQ_SCORE_AUTO && gram_pays(N, K, T, n_alpha, sms)));
+  if (mode == AWQ_SCORE_GRAM) {
+    if (!gram_ok || ws_bytes < L.gram_total) return false;
+    *out = Sched::GRAM;
+    return true;
+  }
+  if (want_gram && ws_bytes >= L.gram_total) *out = Sched::GRAM;
+  else if (ws_bytes >= L.total) *out = Sched::OVERLAP;
+  else if (ws_bytes >= L.min_total) *out = Sched::SERIAL;
+  else return false;
+  return true;
 }
 
 }  // namespace
@@ -553,7 +626,7 @@ size_t search_workspace_min_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alp
   if (check_cfg(cfg) != AWQ_OK || check_nk(N, K, cfg) != AWQ_OK || T < 1 || n_alpha < 1 ||
       n_alpha > 64)
     return 0;
-  return search_layout(N, K, n_alpha).min_total;
+  return search_layout(N, K, T, n_alpha).min_total;
 }
 }  // namespace awq
 
@@ -564,7 +637,24 @@ size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alp
   if (check_cfg(cfg) != AWQ_OK || check_nk(N, K, cfg) != AWQ_OK || T < 1 || n_alpha < 1 ||
       n_alpha > 64)
     return 0;
-  return search_layout(N, K, n_alpha).total;
+  const SearchLayout L = search_layout(N, K, T, n_alpha);
+  int sms = 148;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 148;
+  }
+  Sched sc;
+  if (!pick_schedule(N, K, T, n_alpha, SIZE_MAX, sms, L, &sc)) return 0;
+  return sc == Sched::GRAM ? L.gram_total : L.total;
+}
+
+awq_status_t awq_set_score_mode(awq_score_mode_t mode) {
+  if (mode != AWQ_SCORE_AUTO && mode != AWQ_SCORE_DIRECT && mode != AWQ_SCORE_GRAM)
+    return AWQ_ERR_INVALID_ARG;
+  g_score_mode.store(mode);
+  return AWQ_OK;
 }
 
 awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
@@ -581,11 +671,16 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
       !aligned4(err_out) || !aligned4(best_idx) || (s_out && !aligned16(s_out)) ||
       (inv_s_out && !aligned16(inv_s_out)) || !aligned16(workspace))
     return AWQ_ERR_MISALIGNED;
-  const SearchLayout L = search_layout(N, K, n_alpha);
+  const SearchLayout L = search_layout(N, K, T, n_alpha);
+  if (g_score_mode.load() == AWQ_SCORE_GRAM && !gram_shape_ok(K, T))
+    return AWQ_ERR_UNSUPPORTED_SHAPE;
   if (!workspace || ws_bytes < L.min_total) return AWQ_ERR_WORKSPACE;
-  const bool overlap = ws_bytes >= L.total;
   DeviceInfo* d = nullptr;
   AWQ_TRY(device_info(&d));
+  Sched sched;
+  if (!pick_schedule(N, K, T, n_alpha, ws_bytes, d->sms, L, &sched)) return AWQ_ERR_WORKSPACE;
+  const bool overlap = sched != Sched::SERIAL;
+  const bool use_gram = sched == Sched::GRAM;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -599,10 +694,24 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   const __half* W = static_cast<const __half*>(W_f16);
   const __half* X = static_cast<const __half*>(X_f16);
 
-  CUtensorMap mapX, mapD[2];
-  AWQ_TRY(make_map(&mapX, X, T, K, K, score::BM));
-  AWQ_TRY(make_map(&mapD[0], Dbuf[0], N, K, K, score::BN));
-  AWQ_TRY(make_map(&mapD[1], Dbuf[1], N, K, K, score::BN));
+  unsigned int* hmax = reinterpret_cast<unsigned int*>(ws + L.hmax);
+  float* colsq = reinterpret_cast<float*>(ws + L.colsq);
+  __half* Xt = reinterpret_cast<__half*>(ws + L.xt);
+  __half* Bm = reinterpret_cast<__half*>(ws + L.bmat);
+
+  // direct: A = X tiles, B = D tiles; Gram: A = D tiles, B = tiles of the scaled triangle of H
+  CUtensorMap mapX, mapD[2], mapXa, mapXb, mapBm;
+  if (use_gram) {
+    AWQ_TRY(make_map(&mapXa, Xt, K, L.Tp, L.Tp, gram::BM));
+    AWQ_TRY(make_map(&mapXb, Xt, K, L.Tp, L.Tp, gram::BN));
+    AWQ_TRY(make_map(&mapBm, Bm, K, K, K, gram::BN));
+    AWQ_TRY(make_map(&mapD[0], Dbuf[0], N, K, K, gram::BM));
+    AWQ_TRY(make_map(&mapD[1], Dbuf[1], N, K, K, gram::BM));
+  } else {
+    AWQ_TRY(make_map(&mapX, X, T, K, K, score::BM));
+    AWQ_TRY(make_map(&mapD[0], Dbuf[0], N, K, K, score::BN));
+    AWQ_TRY(make_map(&mapD[1], Dbuf[1], N, K, K, score::BN));
+  }
 
   // 1. statistic
   const float* mp = mean_abs;
@@ -631,12 +740,55 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   prof_start(AWQ_K_ABSMAX, st);
   absmax_kernel<<<agrid, 256, 0, st>>>(W, n8, absmax);
   AWQ_TRY(launched(AWQ_K_ABSMAX, st));
-  // 4. per alpha: residual D = W - Q(W diag s) diag(s)^-1, then sum of squares of X D^T
-  if (cudaFuncSetAttribute(score::score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           score::SMEM_BYTES) != cudaSuccess) {
+  // 4. Gram schedule: X^T and its column sums of squares, max_k H[k][k], then the scaled lower
+  //    triangle of H = X^T X (once per layer)
+  auto smem_attr = [](const void* f, int bytes) -> awq_status_t {
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess)
+      return AWQ_OK;
     cudaGetLastError();
     return AWQ_ERR_CUDA;
+  };
+  gram::Params gp{};
+  int ggrid = 0;
+  if (use_gram) {
+    if (cudaMemsetAsync(hmax, 0, sizeof(unsigned int), st) != cudaSuccess) {
+      cudaGetLastError();
+      return AWQ_ERR_CUDA;
+    }
+    const int nblk = static_cast<int>(L.Tp / gram::TOK_BLOCK);
+    prof_start(AWQ_K_GRAM_PREP, st);
+    gram::transpose_kernel<<<dim3(static_cast<unsigned>(K / 64), static_cast<unsigned>(nblk)), 256,
+                             0, st>>>(X, static_cast<int>(T), static_cast<int>(K),
+                                      static_cast<int>(L.Tp), Xt, colsq);
+    AWQ_TRY(launched(AWQ_K_GRAM_PREP, st));
+    prof_start(AWQ_K_GRAM_PREP, st);
+    gram::colsq_max_kernel<<<static_cast<unsigned>((K + 31) / 32), 256, 0, st>>>(
+        colsq, nblk, static_cast<int>(K), hmax);
+    AWQ_TRY(launched(AWQ_K_GRAM_PREP, st));
+    AWQ_TRY(smem_attr(reinterpret_cast<const void*>(gram::tri_kernel<gram::GRAM>), gram::SMEM_BYTES));
+    AWQ_TRY(smem_attr(reinterpret_cast<const void*>(gram::tri_kernel<gram::SCORE>), gram::SMEM_BYTES));
+    gp.K = static_cast<int>(K);
+    gp.N = static_cast<int>(N);
+    gp.num_kb = nblk;  // TOK_BLOCK == BK: one k-block per token block
+    gp.num_tiles = gram_tiles(K);
+    gp.B = Bm;
+    gp.hmax = hmax;
+    gp.status = d->status;
+    gp.limit_ns = g_wait_limit_ns.load();
+    prof_start(AWQ_K_GRAM, st);
+    gram::tri_kernel<gram::GRAM><<<std::min(gp.num_tiles, d->sms), gram::THREADS,
+                                   gram::SMEM_BYTES, st>>>(mapXa, mapXb, gp);
+    AWQ_TRY(launched(AWQ_K_GRAM, st));
+    gp.row_tiles = static_cast<int>((N + gram::BM - 1) / gram::BM);
+    gp.col_tiles = static_cast<int>((K + gram::BN - 1) / gram::BN);
+    gp.num_tiles = gp.row_tiles * gp.col_tiles;
+    gp.num_kb = 0;
+    gp.B = nullptr;
+    ggrid = std::min(gp.num_tiles, std::min(d->sms, kPartialStride));
+  } else {
+    AWQ_TRY(smem_attr(reinterpret_cast<const void*>(score::score_kernel), score::SMEM_BYTES));
   }
+  // 5. per alpha: residual D = W - Q(W diag s) diag(s)^-1, then its error score
   score::Params sp{};
   sp.tiles_n = static_cast<int>((N + score::BN - 1) / score::BN);
   const int tiles_m = static_cast<int>((T + score::BM - 1) / score::BM);
@@ -676,10 +828,19 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[0], rs)));
   for (int i = 0; i < n_alpha; ++i) {
     if (overlap) AWQ_TRY(ev(cudaStreamWaitEvent(st, d->res_done[i & 1], 0)));
-    sp.partial = partial + static_cast<size_t>(i) * kPartialStride;
-    prof_start(AWQ_K_SCORE, st);
-    score::score_kernel<<<sgrid, score::THREADS, score::SMEM_BYTES, st>>>(mapX, mapD[i & 1], sp);
-    AWQ_TRY(launched(AWQ_K_SCORE, st));
+    if (use_gram) {
+      gp.D = Dbuf[i & 1];
+      gp.partial = partial + static_cast<size_t>(i) * kPartialStride;
+      prof_start(AWQ_K_SCORE_GRAM, st);
+      gram::tri_kernel<gram::SCORE><<<ggrid, gram::THREADS, gram::SMEM_BYTES, st>>>(
+          mapD[i & 1], mapBm, gp);
+      AWQ_TRY(launched(AWQ_K_SCORE_GRAM, st));
+    } else {
+      sp.partial = partial + static_cast<size_t>(i) * kPartialStride;
+      prof_start(AWQ_K_SCORE, st);
+      score::score_kernel<<<sgrid, score::THREADS, score::SMEM_BYTES, st>>>(mapX, mapD[i & 1], sp);
+      AWQ_TRY(launched(AWQ_K_SCORE, st));
+    }
     if (i + 1 < n_alpha) {
       if (overlap) {
         AWQ_TRY(ev(cudaEventRecord(d->score_done[i & 1], st)));
@@ -690,9 +851,10 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
       if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[(i + 1) & 1], rs)));
     }
   }
-  // 5. errors, argmin, winning scales
+  // 6. errors, argmin, winning scales
   prof_start(AWQ_K_FINALIZE, st);
-  finalize_kernel<<<1, 256, 0, st>>>(partial, sgrid, n_alpha, absmax,
+  finalize_kernel<<<1, 256, 0, st>>>(partial, use_gram ? ggrid : sgrid, n_alpha, absmax,
+                                     use_gram ? hmax : nullptr,
                                      static_cast<double>(T) * static_cast<double>(N), s_grid,
                                      inv_grid, static_cast<int>(K), err_out, best_idx, s_out,
                                      inv_s_out);

@@ -37,12 +37,41 @@ def test_status_strings(L):
 
 
 def test_workspace_bytes(L):
-    n = awq.awq_search_workspace_bytes(4096, 4096, 8192, 20)
+    awq.awq_set_score_mode("direct")
+    try:
+        n = awq.awq_search_workspace_bytes(4096, 4096, 8192, 20)
+    finally:
+        awq.awq_set_score_mode("auto")
     assert n >= 2 * 4096 * 4096 * 2      # two fp16 residual buffers (overlapped schedule)
     assert n < 2 * 4096 * 4096 * 2 + (4 << 20)
     assert awq.awq_search_workspace_bytes(4096, 4100, 8192, 20) == 0   # K % G
     assert awq.awq_search_workspace_bytes(4096, 4096, 8192, 65) == 0   # too many alphas
     assert awq.awq_search_workspace_bytes(4096, 4096, 8192, 20, group_size=96) == 0
+
+
+def test_score_mode_and_gram_workspace(L):
+    """AUTO scores through H = X^T X where that takes fewer tensor-core steps: for the
+    4096 x 4096 layer with 8192 tokens the workspace then adds X^T [K, T], the fp16 triangle of
+    H [K, K] and the column sums [T / 64, K]; with 512 tokens the direct product is cheaper."""
+    N = K = 4096
+    T = 8192
+    direct = 2 * N * K * 2
+    gram_extra = K * T * 2 + K * K * 2 + (T // 64) * K * 4
+    n = awq.awq_search_workspace_bytes(N, K, T, 20)
+    assert direct + gram_extra <= n < direct + gram_extra + (4 << 20)
+    small_t = awq.awq_search_workspace_bytes(N, K, 512, 20)
+    assert direct <= small_t < direct + (4 << 20)
+    awq.awq_set_score_mode("gram")
+    try:
+        forced = awq.awq_search_workspace_bytes(N, K, 512, 20)
+        assert direct + K * 512 * 2 + K * K * 2 <= forced < direct + K * 512 * 2 + K * K * 2 + (4 << 20)
+        # T = 1 pads to 64 tokens
+        assert awq.awq_search_workspace_bytes(128, 64, 1, 2, group_size=64) >= 2 * 64 * 64 * 2
+    finally:
+        awq.awq_set_score_mode("auto")
+    with pytest.raises(awq.AwqError):
+        awq.awq_set_score_mode(3)
+    assert awq.awq_search_workspace_bytes(N, K, T, 20) == n
 
 
 def _code(L, fn, *args):

@@ -9,6 +9,8 @@ chosen alpha index exact (unless the oracle's own errors are a near-tie within t
 W4A16 outputs within 2e-2 of max|reference| against the oracle's fp64 dequant-matmul.
 """
 
+import contextlib
+
 import numpy as np
 import pytest
 
@@ -149,7 +151,33 @@ def _score_bound(X16, W16, s_grid, G, sym):
     return np.array(out)
 
 
-def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False):
+def _gram_bound(X16, W16, s_grid, G, sym):
+    """Per-alpha bound on |E_gram - E_exact| for the Gram schedule: D rounded to fp16
+    (2 * 2^-11 of |d|^T A |d|, A = |X|^T |X| >= |H|), H accumulated in fp32 over T tokens
+    (T 2^-24), rounded to fp16 (2^-11), and d^T H' d accumulated in fp32 over K + 256 terms; so
+    per output |dE_n| <= (3 2^-11 + (K + T + 256) 2^-23) |d_n|^T A |d_n|, and
+    sum_n |d_n|^T A |d_n| = || |X| |D|^T ||_F^2."""
+    X = np.abs(X16.astype(np.float64))
+    T, K = X.shape
+    c = 3 * 2.0 ** -11 + (K + T + 256) * 2.0 ** -23
+    out = []
+    for s in s_grid:
+        qd = ref.quantize_pack(W16, s, G, sym)
+        D = W16.astype(np.float64) - ref.dequantize(qd["qweight"], qd["scales"], qd["zeros"], G, s=s)
+        out.append(c * float(np.sum((X @ np.abs(D).T) ** 2)) / (T * W16.shape[0]))
+    return np.array(out)
+
+
+@contextlib.contextmanager
+def score_mode(mode):
+    awq.awq_set_score_mode(mode)
+    try:
+        yield
+    finally:
+        awq.awq_set_score_mode("auto")
+
+
+def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False, gram=False):
     W, X = dev(W16), dev(X16)
     m = awq.calib_stats(X) if use_m else None
     err, best, s, inv_s = awq.search_scale(W, X, alphas, G, sym, mean_abs=m)
@@ -157,8 +185,13 @@ def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False):
     m_gpu = host(awq.calib_stats(X))
     r = ref.search_scale(W16, X16, alphas, G, sym, m=m_gpu)
     e = host(err).astype(np.float64)
-    tol = np.maximum(1e-3 * r["err"], _score_bound(X16, W16, r["s_grid"], G, sym)
-                     if X16.shape[0] * W16.shape[0] < 4096 else 0.0)
+    small = X16.shape[0] * W16.shape[0] < 4096
+    bound = 0.0
+    if small:
+        bound = _score_bound(X16, W16, r["s_grid"], G, sym)
+        if gram:
+            bound = bound + _gram_bound(X16, W16, r["s_grid"], G, sym)
+    tol = np.maximum(1e-3 * r["err"], bound)
     assert np.all(np.abs(e - r["err"]) <= tol), (e, r["err"], tol)
     b = int(host(best)[0])
     if b != r["best"]:   # only a near-tie of the oracle's own errors may pick another alpha
@@ -215,6 +248,60 @@ def test_search_overlapped_schedule_matches_serial():
     awq.awq_stream_status()
     for u, v in zip(a, b):
         assert torch.equal(u, v)
+
+
+GRAM_CASES = [(700, 1664, 333, 128, False), (256, 512, 4000, 64, False),
+              (1000, 1024, 2048, 128, True), (130, 64, 1, 64, False), (33, 4096, 700, 128, False),
+              (129, 320, 64, 64, True)]
+
+
+@pytest.mark.parametrize("N,K,T,G,sym", GRAM_CASES)
+def test_search_gram(N, K, T, G, sym):
+    """Scoring through H = X^T X (forced): errors against the oracle's direct fp64 definition.
+    The cases cover ragged row and column tiles of the triangle (K not a multiple of 256),
+    T = 1 (one token, padded to 64), odd numbers of 128-row H tiles and both group sizes."""
+    d = layer(N * 3 + K + T, N, K, T, n_out=max(1, K // 100))
+    with score_mode("gram"):
+        _check_search(d["W"], d["X"], synth.alpha_grid(20), G, sym, use_m=True, gram=True)
+
+
+def test_search_gram_deterministic_and_close_to_direct():
+    d = layer(21, 1000, 1024, 2048, n_out=10)
+    W, X = dev(d["W"]), dev(d["X"])
+    alphas = synth.alpha_grid(20)
+    with score_mode("gram"):
+        a = awq.search_scale(W, X, alphas)
+        b = awq.search_scale(W, X, alphas)
+    with score_mode("direct"):
+        c = awq.search_scale(W, X, alphas)
+    awq.awq_stream_status()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    eg, ed = host(a[0]).astype(np.float64), host(c[0]).astype(np.float64)
+    np.testing.assert_allclose(eg, ed, rtol=1e-4)
+    bg, bd = int(host(a[1])[0]), int(host(c[1])[0])
+    assert bg == bd or abs(ed[bg] - ed[bd]) <= 1e-4 * ed[bd]
+
+
+def test_search_gram_zero_activations():
+    """X = 0: H = 0, every error 0 and the first alpha wins."""
+    d = layer(22, 256, 512, 300, n_out=4)
+    X16 = np.zeros_like(d["X"])
+    with score_mode("gram"):
+        err, best, s, inv_s = awq.search_scale(dev(d["W"]), dev(X16), synth.alpha_grid(20))
+    awq.awq_stream_status()
+    assert np.all(host(err) == 0) and int(host(best)[0]) == 0
+
+
+def test_search_gram_large_activation_range():
+    """Outlier channels 2^10 above the rest and one token 2^6 above the others: the power-of-two
+    scale of H keeps the small channels' entries in fp16's normal range."""
+    d = layer(23, 384, 1024, 1500, n_out=8, mult=1024.0)
+    X16 = d["X"].astype(np.float32)
+    X16[7] *= 64.0
+    X16 = np.clip(X16, -60000, 60000).astype(np.float16)
+    with score_mode("gram"):
+        _check_search(d["W"], X16, synth.alpha_grid(20), gram=True)
 
 
 @pytest.mark.slow
