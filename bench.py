@@ -129,7 +129,8 @@ def algorithmic(spec, G, n_alpha, gemm_m):
         # Gram schedule: X^T and column sums (read X, write X^T), H's lower triangle (T K (K+1)
         # flops), then per alpha sum_n d_n^T H' d_n: K (K+1) / 2 multiply-adds and a K-long dot
         # per output
-        "gram_prep": {"bytes": 2 * T * K + 2 * ((T + 63) // 64 * 64) * K + 4 * ((T + 63) // 64) * K},
+        "gram_prep": {"bytes": 2 * T * K + 2 * ((T + 63) // 64 * 64) * K + 4 * ((T + 63) // 64) * K,
+                      "launches": 2},   # transpose + column-sum maximum, bytes for both
         "gram": {"flops": T * K * (K + 1)},
         "score_gram": {"flops": N * K * (K + 3)},
         "quantize_pack": {"bytes": 2 * N * K + 4 * K + packed},
@@ -638,7 +639,8 @@ def run_ours(args):
         avg_us = ms_tot * 1e3 / n
         row = {"launches": n, "avg_us": round(avg_us, 3), "share": None}
         if name in alg and "bytes" in alg[name]:
-            row["GB/s"] = round(alg[name]["bytes"] / (avg_us * 1e-6) / 1e9, 1)
+            per = avg_us * alg[name].get("launches", 1)
+            row["GB/s"] = round(alg[name]["bytes"] / (per * 1e-6) / 1e9, 1)
         if name in alg and "flops" in alg[name]:
             row["TFLOP/s"] = round(alg[name]["flops"] / (avg_us * 1e-6) / 1e12, 1)
         kern[name] = row

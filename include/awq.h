@@ -128,11 +128,13 @@ size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alp
  *   inv_s_out[K] fp32 out (may be NULL): 1 / s (IEEE division), the GEMM's inv_s
  * The scales are computed in fp64 and rounded to fp32; the codes behind E(alpha_i) are exactly
  * those awq_quantize_pack produces for s_i.
- * With the two-buffer workspace, the residual kernels run on a second stream owned by the
- * library (one per device, created on the first call on that device together with the events
- * that order it); it forks from `stream` and rejoins it before the call's last kernel, so the
- * whole sequence can be captured in a CUDA graph once that first call has been made. Searches
- * issued concurrently on one device serialise their residual kernels on that stream.
+ * In the OVERLAP schedule (see awq_search_workspace_bytes) the residual kernels run on a second
+ * stream owned by the library (one per device, created on the first call on that device
+ * together with the events that order it); it forks from `stream` and rejoins it before the
+ * call's last kernel, so the whole sequence can be captured in a CUDA graph once that first
+ * call has been made. Searches issued concurrently on one device serialise their residual
+ * kernels on that stream. The GRAM and SERIAL schedules use `stream` alone (GRAM builds each
+ * next residual inside the scoring launch).
  */
 awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
                               int64_t T, const float* mean_abs, const float* alphas,

@@ -388,8 +388,9 @@ awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
   return e != cudaSuccess ? AWQ_ERR_CUDA : rl;
 }
 
-// Sum of the per-CTA partials of every alpha in fixed order, the 2^-2p of the residual scale
-// and the 1/(T N) of the mean; first minimiser in fp64; copy out s and 1/s of the winner.
+// Sum of the per-CTA partials of every alpha in a fixed order (one warp per alpha: lane l adds
+// partials l, l + 32, ..., then a fixed butterfly), the 2^-2p of the residual scale and the
+// 1/(T N) of the mean; first minimiser in fp64; copy out s and 1/s of the winner.
 // With the Gram schedule (hmax != NULL) the partials hold 2^-h sum_n d^T H' d, i.e. half of
 // 2^-h sum_n d^T H d: the factor 2^(1 + h) restores it.
 __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, int nparts,
@@ -402,13 +403,27 @@ __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, in
   __shared__ double e[64];
   __shared__ int best;
   const int p2 = residual_exponent(*absmax);
-  if (threadIdx.x < static_cast<unsigned>(n_alpha)) {
+  const int h = hmax ? 1 + gram::gram_exponent(*hmax) : 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < n_alpha; i += 8) {
     double sum = 0.0;
-    for (int c = 0; c < nparts; ++c) sum += partial[threadIdx.x * kPartialStride + c];
-    const int h = hmax ? 1 + gram::gram_exponent(*hmax) : 0;
-    const double v = ldexp(sum, h - 2 * p2) / tn;
-    e[threadIdx.x] = v;
-    err_out[threadIdx.x] = static_cast<float>(v);
+    for (int c0 = lane; c0 < nparts; c0 += 8 * 32) {  // eight loads in flight, added in order
+      double v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u;
+        v[u] = c < nparts ? partial[i * kPartialStride + c] : 0.0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum += v[u];
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+      const double v = ldexp(sum, h - 2 * p2) / tn;
+      e[i] = v;
+      err_out[i] = static_cast<float>(v);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -419,11 +434,28 @@ __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, in
     *best_idx = b;
   }
   __syncthreads();
-  const float* sb = s_grid + static_cast<long long>(best) * K;
-  const float* ib = inv_grid + static_cast<long long>(best) * K;
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    if (s_out) s_out[k] = sb[k];
-    if (inv_s_out) inv_s_out[k] = ib[k];
+  // K is a multiple of 64 and every buffer 16-byte aligned: copy float4s, four in flight
+  const float4* sb = reinterpret_cast<const float4*>(s_grid + static_cast<long long>(best) * K);
+  const float4* ib = reinterpret_cast<const float4*>(inv_grid + static_cast<long long>(best) * K);
+  const int K4 = K / 4;
+  for (int k0 = threadIdx.x; k0 < K4; k0 += 4 * blockDim.x) {
+    float4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u * blockDim.x;
+      if (k < K4) {
+        a[u] = sb[k];
+        b[u] = ib[k];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u * blockDim.x;
+      if (k < K4) {
+        if (s_out) reinterpret_cast<float4*>(s_out)[k] = a[u];
+        if (inv_s_out) reinterpret_cast<float4*>(inv_s_out)[k] = b[u];
+      }
+    }
   }
 }
 
@@ -750,6 +782,16 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   };
   gram::Params gp{};
   int ggrid = 0;
+  using TriKern = void (*)(CUtensorMap, CUtensorMap, gram::Params);
+  const TriKern tri_gram = cfg.group_size == 128 ? gram::tri_kernel<gram::GRAM, 128>
+                                                 : gram::tri_kernel<gram::GRAM, 64>;
+  const TriKern tri_score = cfg.group_size == 128 ? gram::tri_kernel<gram::SCORE, 128>
+                                                  : gram::tri_kernel<gram::SCORE, 64>;
+  // the residual of candidate i into buffer i % 2
+  auto res_args = [&](int i) {
+    return ResidualArgs{W, s_grid + static_cast<size_t>(i) * K, inv_grid + static_cast<size_t>(i) * K,
+                        absmax, Dbuf[i & 1], static_cast<int>(N), static_cast<int>(K), cfg.symmetric};
+  };
   if (use_gram) {
     if (cudaMemsetAsync(hmax, 0, sizeof(unsigned int), st) != cudaSuccess) {
       cudaGetLastError();
@@ -765,8 +807,8 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     gram::colsq_max_kernel<<<static_cast<unsigned>((K + 31) / 32), 256, 0, st>>>(
         colsq, nblk, static_cast<int>(K), hmax);
     AWQ_TRY(launched(AWQ_K_GRAM_PREP, st));
-    AWQ_TRY(smem_attr(reinterpret_cast<const void*>(gram::tri_kernel<gram::GRAM>), gram::SMEM_BYTES));
-    AWQ_TRY(smem_attr(reinterpret_cast<const void*>(gram::tri_kernel<gram::SCORE>), gram::SMEM_BYTES));
+    AWQ_TRY(smem_attr(reinterpret_cast<const void*>(tri_gram), gram::SMEM_BYTES));
+    AWQ_TRY(smem_attr(reinterpret_cast<const void*>(tri_score), gram::SMEM_BYTES));
     gp.K = static_cast<int>(K);
     gp.N = static_cast<int>(N);
     gp.num_kb = nblk;  // TOK_BLOCK == BK: one k-block per token block
@@ -775,9 +817,11 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     gp.hmax = hmax;
     gp.status = d->status;
     gp.limit_ns = g_wait_limit_ns.load();
+    gp.res = res_args(0);  // candidate 0's residual is built alongside H
+    gp.res_on = 1;
     prof_start(AWQ_K_GRAM, st);
-    gram::tri_kernel<gram::GRAM><<<std::min(gp.num_tiles, d->sms), gram::THREADS,
-                                   gram::SMEM_BYTES, st>>>(mapXa, mapXb, gp);
+    tri_gram<<<std::min(gp.num_tiles, d->sms), gram::THREADS, gram::SMEM_BYTES, st>>>(mapXa, mapXb,
+                                                                                       gp);
     AWQ_TRY(launched(AWQ_K_GRAM, st));
     gp.row_tiles = static_cast<int>((N + gram::BM - 1) / gram::BM);
     gp.col_tiles = static_cast<int>((K + gram::BN - 1) / gram::BN);
@@ -799,14 +843,14 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   const int sgrid = std::min(sp.num_tiles, std::min(d->sms, kPartialStride));
   const dim3 rgrid(static_cast<unsigned>((N + 8 * QROWS - 1) / (8 * QROWS)),
                    static_cast<unsigned>((K / 8 + 31) / 32));
-  // Residual i goes to buffer i % 2. With two buffers the residual of candidate i + 1 runs on
-  // the side stream while candidate i is scored: the scoring GEMM is tensor-bound and leaves
-  // room on every SM for the memory-bound residual blocks. Events order the two streams (the
+  // Residual i goes to buffer i % 2. GRAM: the scoring launch of candidate i builds residual
+  // i + 1 in its own extra warps. DIRECT with two buffers: the residual of candidate i + 1 runs
+  // on the side stream while candidate i is scored (the scoring GEMM is tensor-bound and leaves
+  // room on every SM for the memory-bound residual blocks); events order the two streams (the
   // side stream forks from and rejoins the caller's stream, so the sequence can be captured in
-  // a graph); with one buffer everything runs in order on the caller's stream.
+  // a graph). With one buffer everything runs in order on the caller's stream.
   auto residual = [&](int i, cudaStream_t rs) -> awq_status_t {
-    ResidualArgs ra{W, s_grid + static_cast<size_t>(i) * K, inv_grid + static_cast<size_t>(i) * K,
-                    absmax, Dbuf[i & 1], static_cast<int>(N), static_cast<int>(K), cfg.symmetric};
+    const ResidualArgs ra = res_args(i);
     prof_start(AWQ_K_RESIDUAL, rs);
     if (cfg.group_size == 128)
       residual_kernel<128><<<rgrid, 256, 0, rs>>>(ra);
@@ -819,36 +863,40 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     cudaGetLastError();
     return AWQ_ERR_CUDA;
   };
-  cudaStream_t rs = overlap ? d->side : st;
-  if (overlap) {
-    AWQ_TRY(ev(cudaEventRecord(d->fork, st)));
-    AWQ_TRY(ev(cudaStreamWaitEvent(rs, d->fork, 0)));
-  }
-  AWQ_TRY(residual(0, rs));
-  if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[0], rs)));
-  for (int i = 0; i < n_alpha; ++i) {
-    if (overlap) AWQ_TRY(ev(cudaStreamWaitEvent(st, d->res_done[i & 1], 0)));
-    if (use_gram) {
+  if (use_gram) {
+    // every launch on the caller's stream: each scoring launch also builds the next residual
+    for (int i = 0; i < n_alpha; ++i) {
       gp.D = Dbuf[i & 1];
       gp.partial = partial + static_cast<size_t>(i) * kPartialStride;
+      gp.res_on = i + 1 < n_alpha ? 1 : 0;
+      if (gp.res_on) gp.res = res_args(i + 1);
       prof_start(AWQ_K_SCORE_GRAM, st);
-      gram::tri_kernel<gram::SCORE><<<ggrid, gram::THREADS, gram::SMEM_BYTES, st>>>(
-          mapD[i & 1], mapBm, gp);
+      tri_score<<<ggrid, gram::THREADS, gram::SMEM_BYTES, st>>>(mapD[i & 1], mapBm, gp);
       AWQ_TRY(launched(AWQ_K_SCORE_GRAM, st));
-    } else {
+    }
+  } else {
+    cudaStream_t rs = overlap ? d->side : st;
+    if (overlap) {
+      AWQ_TRY(ev(cudaEventRecord(d->fork, st)));
+      AWQ_TRY(ev(cudaStreamWaitEvent(rs, d->fork, 0)));
+    }
+    AWQ_TRY(residual(0, rs));
+    if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[0], rs)));
+    for (int i = 0; i < n_alpha; ++i) {
+      if (overlap) AWQ_TRY(ev(cudaStreamWaitEvent(st, d->res_done[i & 1], 0)));
       sp.partial = partial + static_cast<size_t>(i) * kPartialStride;
       prof_start(AWQ_K_SCORE, st);
       score::score_kernel<<<sgrid, score::THREADS, score::SMEM_BYTES, st>>>(mapX, mapD[i & 1], sp);
       AWQ_TRY(launched(AWQ_K_SCORE, st));
-    }
-    if (i + 1 < n_alpha) {
-      if (overlap) {
-        AWQ_TRY(ev(cudaEventRecord(d->score_done[i & 1], st)));
-        // buffer (i + 1) % 2 was last read by the scoring of candidate i - 1
-        if (i >= 1) AWQ_TRY(ev(cudaStreamWaitEvent(rs, d->score_done[(i - 1) & 1], 0)));
+      if (i + 1 < n_alpha) {
+        if (overlap) {
+          AWQ_TRY(ev(cudaEventRecord(d->score_done[i & 1], st)));
+          // buffer (i + 1) % 2 was last read by the scoring of candidate i - 1
+          if (i >= 1) AWQ_TRY(ev(cudaStreamWaitEvent(rs, d->score_done[(i - 1) & 1], 0)));
+        }
+        AWQ_TRY(residual(i + 1, rs));
+        if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[(i + 1) & 1], rs)));
       }
-      AWQ_TRY(residual(i + 1, rs));
-      if (overlap) AWQ_TRY(ev(cudaEventRecord(d->res_done[(i + 1) & 1], rs)));
     }
   }
   // 6. errors, argmin, winning scales

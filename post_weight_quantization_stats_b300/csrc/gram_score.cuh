@@ -22,9 +22,15 @@
 // SCORE tiles differ in length (the triangle), so tiles are listed longest first and dealt to
 // the CTAs in a fixed serpentine order (CTA c takes list positions c, 2P-1-c, 2P+c, ...); each
 // CTA's partial sums its tiles in that order, so the result does not depend on timing.
+//
+// Warps 6-13 build the residual of the NEXT candidate meanwhile (the GRAM launch builds
+// candidate 0's, the SCORE launch of candidate i builds candidate i + 1's) into the other of two
+// residual buffers: 8-warp residual blocks (quant.cuh) dealt round-robin over the CTAs. The kernel
+// boundary orders that residual before its own scoring launch, so no launch waits on another.
 #pragma once
 
 #include "awq_device.cuh"
+#include "quant.cuh"
 
 namespace awq {
 namespace gram {
@@ -36,7 +42,9 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
+constexpr int RES_TEAMS = 1;                // 8-warp residual teams
+constexpr int RES_WARPS = 8 * RES_TEAMS;
+constexpr int THREADS = 192 + 32 * RES_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int TOK_BLOCK = 64;  // tokens per transpose block (Tp is a multiple of it)
@@ -54,6 +62,8 @@ struct Params {
   __half* B;                  // GRAM: [K, K] output
   const unsigned int* hmax;   // GRAM: bit pattern of max_k sum_t x_tk^2 (fp32, >= 0)
   double* partial;            // SCORE: [gridDim.x]
+  ResidualArgs res;           // the next candidate's residual (when res_on)
+  int res_on;
   int* status;
   unsigned long long limit_ns;
 };
@@ -104,7 +114,7 @@ __device__ __forceinline__ float2 h2f2(uint32_t w) {
   return __half22float2(h);
 }
 
-template <int MODE>
+template <int MODE, int G>
 __global__ void __launch_bounds__(THREADS, 1)
     tri_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                Params p) {
@@ -203,6 +213,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       mma_commit(drain);  // every MMA issued above has finished once this arrives
       wait_drain(drain, 0, p.limit_ns);
     }
+  } else if (warp >= 6) {
+    if (p.res_on) {
+      // team tm of 8 warps takes blocks cta * RES_TEAMS + tm, + P * RES_TEAMS, ...; the next
+      // block's loads are issued before this block's arithmetic
+      const int tm = (warp - 6) >> 3, rw = (warp - 6) & 7;
+      const int chunks = (p.res.K / 8 + 31) / 32;
+      const int items = (p.res.N + 8 * QROWS - 1) / (8 * QROWS) * chunks;
+      const int stride = P * RES_TEAMS;
+      const float p2 = ldexpf(1.0f, residual_exponent(*p.res.absmax));
+      int item = cta * RES_TEAMS + tm;
+      ResidualRegs cur, nxt;
+      if (item < items) residual_load(p.res, item / chunks, item % chunks, rw, lane, cur);
+      for (; item < items; item += stride) {
+        const int next = item + stride;
+        if (next < items) residual_load(p.res, next / chunks, next % chunks, rw, lane, nxt);
+        residual_store<G>(p.res, cur, p2);
+        if (next < items) cur = nxt;
+      }
+    }
   } else {
     const uint32_t q = static_cast<uint32_t>(warp & 3);  // TMEM lane quarter of this warp
     const uint32_t lane_base = tmem_base + ((q * 32u) << 16);
@@ -218,14 +247,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int col0 = t.rb * BN;
       const uint32_t acc = local & 1u, use = local >> 1;
       if (MODE == SCORE) {
-        // this row's D[n][col0 .. col0 + 255], fetched while the tile's MMAs run
-        uint4 dv[BN / 8];
+        // this row's D[n][col0 .. col0 + 255] in 32-column chunks; chunks c and c + 4 share a
+        // slot, so the first 128 columns are fetched while the tile's MMAs run and chunk c + 4
+        // as soon as chunk c is used
         const bool rok = row < p.N;
         const __half* drow = p.D + static_cast<long long>(rok ? row : 0) * p.K + col0;
+        auto ld = [&](int v) -> uint4 {
+          return (rok && col0 + v * 8 < p.K) ? __ldg(reinterpret_cast<const uint4*>(drow + v * 8))
+                                             : make_uint4(0u, 0u, 0u, 0u);
+        };
+        uint4 dv[16];
 #pragma unroll
-        for (int v = 0; v < BN / 8; ++v)
-          dv[v] = (rok && col0 + v * 8 < p.K) ? __ldg(reinterpret_cast<const uint4*>(drow + v * 8))
-                                              : make_uint4(0u, 0u, 0u, 0u);
+        for (int v = 0; v < 16; ++v) dv[v] = ld(v);
         const bool got = wait_bounded(&tfull[acc], use & 1u, wc);
         if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld is .sync.aligned
         tc_fence_after();
@@ -237,7 +270,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 w = dv[c * 4 + v];
+            const uint4 w = dv[(c & 3) * 4 + v];
+            if (c < 4) dv[(c & 3) * 4 + v] = ld((c + 4) * 4 + v);
             const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -301,45 +335,68 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // X [T, K] fp16 (row stride K) -> Xt [K, Tp] fp16 with zero columns t >= T, and
 // colsq[tb][k] = sum of x_tk^2 over the 64 tokens of block tb (fp32, fixed order).
-// Grid (K / 64, Tp / 64), 256 threads.
+// Grid (K / 64, Tp / 64), 256 threads. Thread i reads channels 8 (i % 8) .. + 7 of tokens
+// 2 (i / 8) and 2 (i / 8) + 1 (a warp reads eight whole 128-byte row pieces) and keeps them in
+// shared memory as token pairs: tw[k][p] holds (x[2p][k], x[2p+1][k]), rows of 33 words, so the
+// pair stores conflict at most two-way and the row reads below not at all. Thread i then
+// writes tokens 16 (i % 4) .. + 15 of channel i / 4 (a warp writes eight 128-byte row pieces).
 __global__ void __launch_bounds__(256) transpose_kernel(const __half* __restrict__ X, int T, int K,
                                                         int Tp, __half* __restrict__ Xt,
                                                         float* __restrict__ colsq) {
-  __shared__ __align__(16) __half tile[TOK_BLOCK][64 + 8];  // [t][k]
-  __shared__ float part[4][64];
+  __shared__ uint32_t tw[64][33];
+  __shared__ float part[8][64];
   const int k0 = blockIdx.x * 64, t0 = blockIdx.y * TOK_BLOCK;
-  const int tid = threadIdx.x;
-  for (int i = tid; i < TOK_BLOCK * 8; i += 256) {
-    const int tr = i >> 3, ch = i & 7;
-    const int t = t0 + tr;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (t < T) v = __ldg(reinterpret_cast<const uint4*>(X + static_cast<long long>(t) * K + k0 + ch * 8));
-    *reinterpret_cast<uint4*>(&tile[tr][ch * 8]) = v;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const int c8 = tid & 7, q = tid >> 3;
+    const int ta = t0 + 2 * q, tb = ta + 1;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 ra = ta < T ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<long long>(ta) * K + k0 + c8 * 8)) : zero;
+    const uint4 rb = tb < T ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<long long>(tb) * K + k0 + c8 * 8)) : zero;
+    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+    float sq[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __half2 ha, hb;
+      memcpy(&ha, &wa[j], 4);
+      memcpy(&hb, &wb[j], 4);
+      const __half2 lo = __lows2half2(ha, hb), hi = __highs2half2(ha, hb);  // (a_k, b_k)
+      uint32_t ulo, uhi;
+      memcpy(&ulo, &lo, 4);
+      memcpy(&uhi, &hi, 4);
+      tw[c8 * 8 + 2 * j][q] = ulo;
+      tw[c8 * 8 + 2 * j + 1][q] = uhi;
+      const float2 fa = __half22float2(ha), fb = __half22float2(hb);
+      sq[2 * j] = fmaf(fb.x, fb.x, fa.x * fa.x);
+      sq[2 * j + 1] = fmaf(fb.y, fb.y, fa.y * fa.y);
+    }
+    // lanes with the same c8 (xor 8, 16) hold the warp's 8 tokens of these channels
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sq[j] += __shfl_xor_sync(0xffffffffu, sq[j], 8);
+      sq[j] += __shfl_xor_sync(0xffffffffu, sq[j], 16);
+    }
+    if (lane < 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part[warp][c8 * 8 + j] = sq[j];
+    }
   }
   __syncthreads();
   {
-    const int col = tid & 63, pr = tid >> 6;
-    float s = 0.f;
+    const int k = tid >> 2, w4 = tid & 3;
+    uint32_t v[8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float x = __half2float(tile[pr * 16 + r][col]);
-      s = fmaf(x, x, s);
-    }
-    part[pr][col] = s;
+    for (int c = 0; c < 8; ++c) v[c] = tw[k][w4 * 8 + c];
+    uint4* dst = reinterpret_cast<uint4*>(Xt + static_cast<long long>(k0 + k) * Tp + t0 + w4 * 16);
+    dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
   }
-  // a warp covers 32 consecutive channels of one 8-token chunk: conflict-free shared reads
-  for (int i = tid; i < 64 * 8; i += 256) {
-    const int kr = i & 63, ch = i >> 6;
-    __align__(16) __half o[8];
+  if (tid < 64) {
+    float s2 = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = tile[ch * 8 + e][kr];
-    *reinterpret_cast<uint4*>(Xt + static_cast<long long>(k0 + kr) * Tp + t0 + ch * 8) =
-        *reinterpret_cast<const uint4*>(o);
+    for (int w = 0; w < 8; ++w) s2 += part[w][tid];
+    colsq[static_cast<long long>(blockIdx.y) * K + k0 + tid] = s2;
   }
-  __syncthreads();
-  if (tid < 64)
-    colsq[static_cast<long long>(blockIdx.y) * K + k0 + tid] =
-        ((part[0][tid] + part[1][tid]) + part[2][tid]) + part[3][tid];
 }
 
 // hmax = max_k sum_tb colsq[tb][k] as fp32 bits (each channel's sum in fixed order; the max of

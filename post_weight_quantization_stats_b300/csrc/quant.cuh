@@ -26,24 +26,30 @@ struct GroupParams {
   float rcp;   // 1 / step, correctly rounded
 };
 
+__device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric);
+
 // Group step and zero point; TEAM = G / 8 consecutive lanes hold one group.
 template <int TEAM>
 __device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool symmetric) {
-  float lo = wp[0], hi = wp[0], amax = fabsf(wp[0]);
+  float lo = wp[0], hi = wp[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) {
     lo = fminf(lo, wp[i]);
     hi = fmaxf(hi, wp[i]);
-    amax = fmaxf(amax, fabsf(wp[i]));
   }
 #pragma unroll
   for (int o = TEAM / 2; o >= 1; o >>= 1) {
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   }
+  return group_params_of(lo, hi, symmetric);
+}
+
+// Step, zero point and reciprocal of a group from the min and max of its w'.
+__device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric) {
   GroupParams g;
   if (symmetric) {
+    const float amax = fmaxf(hi, -lo);  // max |w'| of the group
     float st = __fdiv_rn(amax, 8.0f);
     if (st == 0.0f) st = 1.0f;
     g.step = st;
@@ -63,27 +69,38 @@ __device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool s
   return g;
 }
 
+// Round to the nearest integer, ties to even, for |x| < 2^22: x + 1.5 * 2^23 lies in a binade
+// whose unit in the last place is 1, so that IEEE addition rounds x itself (1.5 * 2^23 is even,
+// so ties land on even integers) and the subtraction is exact. Two full-rate adds.
+__device__ __forceinline__ float rint_small(float x) {
+  return __fsub_rn(__fadd_rn(x, 0x1.8p23f), 0x1.8p23f);
+}
+
 // rint(fl32(wp / step)) without a division in the common case. |wp / step| <= 15 for every
 // weight of the group, so t = fl32(wp * fl32(1 / step)) is within 2^-19 of the exact quotient
 // and fl32 of the quotient within 2^-20 of it: unless t lies within 2^-17 of a half-integer (a
-// rounding boundary of rint), t and the IEEE quotient round to the same integer. Near a
-// boundary (about 1.5e-5 of all weights) the quotient is computed with IEEE division.
+// rounding boundary of rint), t and the IEEE quotient round to the same integer. With
+// r = rint(t), t - r is exact and t is that close to a half-integer exactly when
+// |t - r| >= 1/2 - 2^-17; there (about 1.5e-5 of all weights) the quotient is computed with
+// IEEE division.
 __device__ __forceinline__ float rint_quotient(float wp, const GroupParams& g) {
   const float t = __fmul_rn(wp, g.rcp);
-  const float f = __fsub_rn(t, floorf(t));
-  if (fabsf(__fsub_rn(f, 0.5f)) <= 0x1p-17f) return rintf(__fdiv_rn(wp, g.step));
-  return rintf(t);
+  const float r = rint_small(t);
+  if (fabsf(__fsub_rn(t, r)) >= 0.5f - 0x1p-17f) return rintf(__fdiv_rn(wp, g.step));
+  return r;
 }
 
-// Stored code (0..15) of one scaled weight.
+// Stored code (0..15) of one scaled weight, as an exact float.
+__device__ __forceinline__ float code_f(float wp, const GroupParams& g, bool symmetric) {
+  const float r = rint_quotient(wp, g);
+  if (symmetric) return __fadd_rn(fminf(fmaxf(r, -8.0f), 7.0f), 8.0f);
+  return fminf(fmaxf(__fadd_rn(r, g.zero), 0.0f), 15.0f);
+}
+
+// The same code as an integer: the low bits of fl32(code + 2^23), whose unit in the last
+// place is 1 (no float-to-integer conversion instruction).
 __device__ __forceinline__ uint32_t code_of(float wp, const GroupParams& g, bool symmetric) {
-  float r = rint_quotient(wp, g);
-  if (symmetric) {
-    r = fminf(fmaxf(r, -8.0f), 7.0f) + 8.0f;
-  } else {
-    r = fminf(fmaxf(__fadd_rn(r, g.zero), 0.0f), 15.0f);
-  }
-  return static_cast<uint32_t>(r);
+  return __float_as_uint(__fadd_rn(code_f(wp, g, symmetric), 0x1p23f)) & 0xFu;
 }
 
 // ------------------------------------------------------------------ quantize + pack kernel
@@ -191,17 +208,27 @@ __global__ void __launch_bounds__(256) scale_grid_kernel(GridArgs a) {
 
 // max |W| over the whole matrix, as the bit pattern of a non-negative float (atomicMax on
 // unsigned int orders non-negative floats correctly; the result is order-independent).
+// Four 16-byte loads in flight per thread per step.
 __global__ void __launch_bounds__(256) absmax_kernel(const __half* __restrict__ W, long long n8,
                                                      unsigned int* out) {
   float m = 0.f;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(W) + i);
-    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n8;
+       i0 += 4 * stride) {
+    uint4 raw[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __half22float2(__habs2(h2[j]));
-      m = fmaxf(m, fmaxf(f.x, f.y));
+    for (int u = 0; u < 4; ++u) {
+      const long long i = i0 + u * stride;
+      raw[u] = i < n8 ? __ldg(reinterpret_cast<const uint4*>(W) + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw[u]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(__habs2(h2[j]));
+        m = fmaxf(m, fmaxf(f.x, f.y));
+      }
     }
   }
 #pragma unroll
@@ -235,49 +262,74 @@ struct ResidualArgs {
 // so either the error is at most step/(2 s) <= |w| or it equals |w|; a clamped code sits at
 // least 7.5 steps out, where the one-step error is below |w'| too. Hence 2^p max|W| < 2^14
 // keeps every residual inside the fp16 range.
-template <int G>
-__global__ void __launch_bounds__(256) residual_kernel(ResidualArgs a) {
-  constexpr int TEAM = G / 8;
-  const int kw = a.K >> 3;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int w = blockIdx.y * 32 + lane;
-  const bool wok = w < kw;
-  const int k0 = (wok ? w : 0) * 8;
-  const int rbase = (blockIdx.x * 8 + warp) * QROWS;
-  float sv[8], iv[8];
-  load8f(a.s + k0, wok, 1.0f, sv);
-  load8f(a.inv_s + k0, wok, 1.0f, iv);
+// One 8-warp block of the residual: warp `warp` (0..7) covers rows (rb * 8 + warp) * QROWS ..
+// + QROWS - 1, lane `lane` the packed word 32 chunk + lane of each. Split into the loads
+// (residual_load: the lane's QROWS weight words and 8 channels of s and 1/s) and the rest
+// (residual_store), so a caller can overlap the next block's loads with this block's work.
+struct ResidualRegs {
   uint4 raw[QROWS];
+  float sv[8], iv[8];
+  int rbase, k0;
+  bool wok;
+};
+
+__device__ __forceinline__ void residual_load(const ResidualArgs& a, int rb, int chunk, int warp,
+                                              int lane, ResidualRegs& r) {
+  const int w = chunk * 32 + lane;
+  r.wok = w < (a.K >> 3);
+  r.k0 = (r.wok ? w : 0) * 8;
+  r.rbase = (rb * 8 + warp) * QROWS;
+  load8f(a.s + r.k0, r.wok, 1.0f, r.sv);
+  load8f(a.inv_s + r.k0, r.wok, 1.0f, r.iv);
 #pragma unroll
-  for (int r = 0; r < QROWS; ++r) {
-    const int row = rbase + r;
-    raw[r] = (wok && row < a.N)
-                 ? __ldg(reinterpret_cast<const uint4*>(a.W + static_cast<long long>(row) * a.K + k0))
-                 : make_uint4(0, 0, 0, 0);
+  for (int q = 0; q < QROWS; ++q) {
+    const int row = r.rbase + q;
+    r.raw[q] = (r.wok && row < a.N)
+                   ? __ldg(reinterpret_cast<const uint4*>(a.W + static_cast<long long>(row) * a.K + r.k0))
+                   : make_uint4(0, 0, 0, 0);
   }
+}
+
+template <int G>
+__device__ __forceinline__ void residual_store(const ResidualArgs& a, const ResidualRegs& r,
+                                               float p2) {
+  constexpr int TEAM = G / 8;
   const bool sym = a.symmetric != 0;
-  const float p2 = ldexpf(1.0f, residual_exponent(*a.absmax));
 #pragma unroll
-  for (int r = 0; r < QROWS; ++r) {
-    const int row = rbase + r;
+  for (int q = 0; q < QROWS; ++q) {
+    const int row = r.rbase + q;
     float wv[8], wp[8];
-    unpack8(raw[r], wv);
+    unpack8(r.raw[q], wv);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wp[i] = __fmul_rn(wv[i], sv[i]);
+    for (int i = 0; i < 8; ++i) wp[i] = __fmul_rn(wv[i], r.sv[i]);
     const GroupParams g = group_params<TEAM>(wp, sym);   // every lane takes part in the shuffles
-    if (wok && row < a.N) {
+    if (r.wok && row < a.N) {
       const float step16 = __half2float(__float2half_rn(g.step));
-      __align__(16) __half out[8];
+      uint32_t out[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float qz = static_cast<float>(code_of(wp[i], g, sym)) - g.zero;  // exact
-        const float w_hat = __fmul_rn(__fmul_rn(qz, step16), iv[i]);
-        out[i] = __float2half_rn(__fmul_rn(__fsub_rn(wv[i], w_hat), p2));
+      for (int i = 0; i < 8; i += 2) {
+        float d2[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float qz = __fsub_rn(code_f(wp[i + j], g, sym), g.zero);  // exact
+          const float w_hat = __fmul_rn(__fmul_rn(qz, step16), r.iv[i + j]);
+          d2[j] = __fmul_rn(__fsub_rn(wv[i + j], w_hat), p2);
+        }
+        const __half2 h = __floats2half2_rn(d2[0], d2[1]);
+        memcpy(&out[i / 2], &h, sizeof(uint32_t));
       }
-      *reinterpret_cast<uint4*>(a.D + static_cast<long long>(row) * a.K + k0) =
-          *reinterpret_cast<const uint4*>(out);
+      *reinterpret_cast<uint4*>(a.D + static_cast<long long>(row) * a.K + r.k0) =
+          make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
+}
+
+// Row blocks of 8 * QROWS rows on grid x, 256-channel column chunks on grid y.
+template <int G>
+__global__ void __launch_bounds__(256) residual_kernel(ResidualArgs a) {
+  ResidualRegs r;
+  residual_load(a, blockIdx.x, blockIdx.y, threadIdx.x >> 5, threadIdx.x & 31, r);
+  residual_store<G>(a, r, ldexpf(1.0f, residual_exponent(*a.absmax)));
 }
 
 }  // namespace awq
