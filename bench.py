@@ -133,6 +133,8 @@ def algorithmic(spec, G, n_alpha, gemm_m):
                       "launches": 2},   # transpose + column-sum maximum, bytes for both
         "gram": {"flops": T * K * (K + 1)},
         "score_gram": {"flops": N * K * (K + 3)},
+        # the persistent launch: H's triangle and every alpha's score
+        "gram_search": {"flops": T * K * (K + 1) + n_alpha * N * K * (K + 3)},
         "quantize_pack": {"bytes": 2 * N * K + 4 * K + packed},
         "gemv": {m: {"bytes": packed + 2 * m * K + 2 * m * N + 4 * K, "flops": 2 * m * N * K}
                  for m in gemm_m},
@@ -698,6 +700,10 @@ def run_ours(args):
 
 # kernel name -> (kernel description, bound, committed ncu summary, source file)
 ROOFLINE_KERNELS = {
+    "gram_search": ("search_kernel: one persistent cooperative launch, tcgen05 kind::f16 X^T X "
+                    "triangle then D B^T over the triangle per alpha, next residual built in "
+                    "extra warps", "tensor", "gram_search_llama7b_attn_4096.md",
+                    "gram_persistent.cuh"),
     "score_gram": ("tri_kernel<SCORE>: tcgen05 kind::f16 D B^T over the triangle, fp32 "
                    "accumulate, d . (D B^T) epilogue", "tensor",
                    "score_gram_llama7b_attn_4096.md", "gram_score.cuh"),

@@ -89,11 +89,20 @@ awq_status_t awq_calib_stats(const void* X_f16, int64_t T, int64_t K, int64_t ld
  *           flops) and stored as fp16 after a power-of-two scale; each candidate then takes
  *           about 2 N K^2 / 2 flops over the lower triangle of H. Equal to DIRECT in exact
  *           arithmetic, so the errors agree to rounding (fp16 H: relative 2^-11 per entry).
+ *           Runs as one persistent cooperative launch (one CTA per SM) over H and every
+ *           candidate; if the device refuses the cooperative launch, as GRAM_LAUNCHES.
+ *   GRAM_LAUNCHES  the same arithmetic with one launch for H and one per candidate (same
+ *           results, bit for bit).
  *   AUTO    GRAM when it takes fewer tensor-core steps (long calibration sets, T > K / 2 or
  *           so), the workspace holds it, and K T, K K < 2^31; DIRECT otherwise.
  * Returns AWQ_ERR_INVALID_ARG for any other value.
  */
-typedef enum { AWQ_SCORE_AUTO = 0, AWQ_SCORE_DIRECT = 1, AWQ_SCORE_GRAM = 2 } awq_score_mode_t;
+typedef enum {
+  AWQ_SCORE_AUTO = 0,
+  AWQ_SCORE_DIRECT = 1,
+  AWQ_SCORE_GRAM = 2,
+  AWQ_SCORE_GRAM_LAUNCHES = 3
+} awq_score_mode_t;
 awq_status_t awq_set_score_mode(awq_score_mode_t mode);
 
 /*
@@ -221,9 +230,10 @@ typedef enum {
   AWQ_K_GEMV = 7,        /* awq_w4a16_gemm, CUDA-core kernel for M <= 2 */
   AWQ_K_GEMM_TC = 8,     /* awq_w4a16_gemm, tcgen05 kernels for larger M */
   AWQ_K_GRAM_PREP = 9,   /* search, GRAM: X^T, column sums of squares and their maximum */
-  AWQ_K_GRAM = 10,       /* search, GRAM: tcgen05 lower triangle of H = X^T X, fp16 */
-  AWQ_K_SCORE_GRAM = 11, /* search, GRAM: tcgen05 sum_n d_n^T H d_n of one alpha */
-  AWQ_K_COUNT = 12
+  AWQ_K_GRAM = 10,       /* search, GRAM_LAUNCHES: tcgen05 lower triangle of H = X^T X, fp16 */
+  AWQ_K_SCORE_GRAM = 11, /* search, GRAM_LAUNCHES: tcgen05 sum_n d_n^T H d_n of one alpha */
+  AWQ_K_GRAM_SEARCH = 12, /* search, GRAM: persistent launch over H and every alpha */
+  AWQ_K_COUNT = 13
 } awq_kernel_id_t;
 
 /*

@@ -64,8 +64,8 @@ _SIGNATURES = {
 }
 
 KERNELS = ("calib_stats", "scale_grid", "absmax", "residual", "score", "finalize",
-           "quantize_pack", "gemv", "gemm_tc", "gram_prep", "gram", "score_gram")
-SCORE_MODES = {"auto": 0, "direct": 1, "gram": 2}
+           "quantize_pack", "gemv", "gemm_tc", "gram_prep", "gram", "score_gram", "gram_search")
+SCORE_MODES = {"auto": 0, "direct": 1, "gram": 2, "gram_launches": 3}
 
 _lib = None
 
@@ -182,7 +182,8 @@ def awq_set_wait_limit_ns(limit_ns: int) -> int:
 
 
 def awq_set_score_mode(mode):
-    """Process-wide choice of how the search scores candidates: "auto", "direct" or "gram"."""
+    """Process-wide choice of how the search scores candidates: "auto", "direct", "gram" or
+    "gram_launches"."""
     _check("awq_set_score_mode", lib().awq_set_score_mode(SCORE_MODES.get(mode, mode)))
 
 

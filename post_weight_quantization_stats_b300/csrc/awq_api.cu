@@ -18,6 +18,7 @@
 #include "../../include/awq.h"
 #include "awq_device.cuh"
 #include "calib_stats.cuh"
+#include "gram_persistent.cuh"
 #include "gram_score.cuh"
 #include "quant.cuh"
 #include "score_gemm.cuh"
@@ -161,6 +162,15 @@ void prof_start(int kernel, cudaStream_t st) {
   }
   g_prof_pending = p.stop;
   ++g_prof_used;
+}
+
+// Drops the event pair prof_start() opened for a launch that did not happen.
+void prof_cancel() {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof_pending) {
+    g_prof_pending = nullptr;
+    --g_prof_used;
+  }
 }
 
 awq_status_t launched(int /*kernel*/, cudaStream_t st) {
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, in
 
 struct SearchLayout {
   size_t m, s_grid, inv_grid, absmax, partial, D, D2, min_total, total;
-  size_t hmax, colsq, xt, bmat, gram_total;   // Gram schedule: H from X^T, its scaled triangle
+  size_t hmax, colsq, xt, bmat, sync, gram_total;  // Gram schedule: H from X^T, its triangle
   int64_t Tp;
 };
 
@@ -484,6 +494,7 @@ SearchLayout search_layout(int64_t N, int64_t K, int64_t T, int32_t n_alpha) {
   L.colsq = off;    off = align256(off + sizeof(float) * (L.Tp / gram::TOK_BLOCK) * K);
   L.xt = off;       off = align256(off + sizeof(__half) * K * L.Tp);
   L.bmat = off;     off = align256(off + sizeof(__half) * K * K);
+  L.sync = off;     off = align256(off + sizeof(unsigned int) * (2 * n_alpha + 1));
   L.gram_total = off;  // Gram schedule (two residual buffers as well)
   return L;
 }
@@ -525,6 +536,18 @@ bool gram_pays(int64_t N, int64_t K, int64_t T, int32_t n_alpha, int sms) {
   return static_cast<double>(n_alpha) * per_alpha + once < static_cast<double>(n_alpha) * direct;
 }
 
+// The persistent Gram-schedule search (gram_persistent.cuh): one cooperative launch, one CTA per
+// SM, after the counters it synchronises on are zeroed. *done is false (and nothing is left
+// pending) when the device refuses the cooperative launch; the caller then takes the
+// one-launch-per-phase path.
+awq_status_t launch_search_persistent(int G, DeviceInfo* d, const SearchLayout& L, uint8_t* ws,
+                                      const __half* Xt, __half* Bm, const unsigned int* hmax,
+                                      __half* const* Dbuf, const __half* W,
+                                      const unsigned int* absmax, const float* s_grid,
+                                      const float* inv_grid, double* partial, int64_t N,
+                                      int64_t K, int n_alpha, int symmetric, bool* done,
+                                      cudaStream_t st);
+
 // The schedule a search with `ws_bytes` of workspace takes (ws_bytes = SIZE_MAX: the one the
 // library prefers). Returns false if the workspace is too small.
 enum class Sched { SERIAL, OVERLAP, GRAM };
@@ -532,9 +555,10 @@ bool pick_schedule(int64_t N, int64_t K, int64_t T, int32_t n_alpha, size_t ws_b
                    const SearchLayout& L, Sched* out) {
   const int mode = g_score_mode.load();
   const bool gram_ok = gram_shape_ok(K, T);
-  const bool want_gram = gram_ok && (mode == AWQ_SCORE_GRAM ||
+  const bool forced = mode == AWQ_SCORE_GRAM || mode == AWQ_SCORE_GRAM_LAUNCHES;
+  const bool want_gram = gram_ok && (forced ||
                                      (mode == AWQ_SCORE_AUTO && gram_pays(N, K, T, n_alpha, sms)));
-  if (mode == AWQ_SCORE_GRAM) {
+  if (forced) {
     if (!gram_ok || ws_bytes < L.gram_total) return false;
     *out = Sched::GRAM;
     return true;
@@ -544,6 +568,84 @@ bool pick_schedule(int64_t N, int64_t K, int64_t T, int32_t n_alpha, size_t ws_b
   else if (ws_bytes >= L.min_total) *out = Sched::SERIAL;
   else return false;
   return true;
+}
+
+awq_status_t launch_search_persistent(int G, DeviceInfo* d, const SearchLayout& L, uint8_t* ws,
+                                      const __half* Xt, __half* Bm, const unsigned int* hmax,
+                                      __half* const* Dbuf, const __half* W,
+                                      const unsigned int* absmax, const float* s_grid,
+                                      const float* inv_grid, double* partial, int64_t N,
+                                      int64_t K, int n_alpha, int symmetric, bool* done,
+                                      cudaStream_t st) {
+  *done = false;
+  CUtensorMap mXa, mXb, mD0, mD1, mB;
+  AWQ_TRY(make_map(&mXa, Xt, K, L.Tp, L.Tp, gram::BM));
+  AWQ_TRY(make_map(&mXb, Xt, K, L.Tp, L.Tp, gram::BN));
+  AWQ_TRY(make_map(&mD0, Dbuf[0], N, K, K, gram::BM));
+  AWQ_TRY(make_map(&mD1, Dbuf[1], N, K, K, gram::BM));
+  AWQ_TRY(make_map(&mB, Bm, K, K, K, gram::BN));
+  gram::SearchParams sp{};
+  sp.K = static_cast<int>(K);
+  sp.N = static_cast<int>(N);
+  sp.n_alpha = n_alpha;
+  sp.gram_tiles = gram_tiles(K);
+  sp.gram_kb = static_cast<int>(L.Tp / gram::BK);
+  sp.row_tiles = static_cast<int>((N + gram::BM - 1) / gram::BM);
+  sp.col_tiles = static_cast<int>((K + gram::BN - 1) / gram::BN);
+  sp.B = Bm;
+  sp.hmax = hmax;
+  sp.D[0] = Dbuf[0];
+  sp.D[1] = Dbuf[1];
+  sp.res = ResidualArgs{W, nullptr, nullptr, absmax, nullptr, static_cast<int>(N),
+                        static_cast<int>(K), symmetric};
+  sp.s_grid = s_grid;
+  sp.inv_grid = inv_grid;
+  sp.partial = partial;
+  sp.pstride = kPartialStride;
+  sp.sync = reinterpret_cast<unsigned int*>(ws + L.sync);
+  sp.status = d->status;
+  sp.limit_ns = g_wait_limit_ns.load();
+  auto kern = G == 128 ? gram::search_kernel<128> : gram::search_kernel<64>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gram::SMEM_BYTES) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return AWQ_ERR_CUDA;
+  }
+  // every CTA must be resident at once: one per SM (the shared memory allows no second)
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, gram::THREADS,
+                                                    gram::SMEM_BYTES) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    return AWQ_OK;  // not launchable cooperatively here: the caller falls back
+  }
+  if (cudaMemsetAsync(sp.sync, 0, sizeof(unsigned int) * (2 * n_alpha + 1), st) != cudaSuccess) {
+    cudaGetLastError();
+    return AWQ_ERR_CUDA;
+  }
+  const int grid = std::min(d->sms, kPartialStride);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(gram::THREADS);
+  cfg.dynamicSmemBytes = gram::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_start(AWQ_K_GRAM_SEARCH, st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mXa, mXb, mD0, mD1, mB, sp);
+  if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported) {
+    cudaGetLastError();
+    prof_cancel();
+    return AWQ_OK;  // the caller falls back
+  }
+  const awq_status_t rl = launched(AWQ_K_GRAM_SEARCH, st);
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  AWQ_TRY(rl);
+  *done = true;
+  return AWQ_OK;
 }
 
 }  // namespace
@@ -683,7 +785,8 @@ size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alp
 }
 
 awq_status_t awq_set_score_mode(awq_score_mode_t mode) {
-  if (mode != AWQ_SCORE_AUTO && mode != AWQ_SCORE_DIRECT && mode != AWQ_SCORE_GRAM)
+  if (mode != AWQ_SCORE_AUTO && mode != AWQ_SCORE_DIRECT && mode != AWQ_SCORE_GRAM &&
+      mode != AWQ_SCORE_GRAM_LAUNCHES)
     return AWQ_ERR_INVALID_ARG;
   g_score_mode.store(mode);
   return AWQ_OK;
@@ -704,7 +807,9 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
       (inv_s_out && !aligned16(inv_s_out)) || !aligned16(workspace))
     return AWQ_ERR_MISALIGNED;
   const SearchLayout L = search_layout(N, K, T, n_alpha);
-  if (g_score_mode.load() == AWQ_SCORE_GRAM && !gram_shape_ok(K, T))
+  const int score_mode = g_score_mode.load();
+  if ((score_mode == AWQ_SCORE_GRAM || score_mode == AWQ_SCORE_GRAM_LAUNCHES) &&
+      !gram_shape_ok(K, T))
     return AWQ_ERR_UNSUPPORTED_SHAPE;
   if (!workspace || ws_bytes < L.min_total) return AWQ_ERR_WORKSPACE;
   DeviceInfo* d = nullptr;
@@ -782,6 +887,7 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   };
   gram::Params gp{};
   int ggrid = 0;
+  bool persistent = false;
   using TriKern = void (*)(CUtensorMap, CUtensorMap, gram::Params);
   const TriKern tri_gram = cfg.group_size == 128 ? gram::tri_kernel<gram::GRAM, 128>
                                                  : gram::tri_kernel<gram::GRAM, 64>;
@@ -807,11 +913,18 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     gram::colsq_max_kernel<<<static_cast<unsigned>((K + 31) / 32), 256, 0, st>>>(
         colsq, nblk, static_cast<int>(K), hmax);
     AWQ_TRY(launched(AWQ_K_GRAM_PREP, st));
+    if (score_mode != AWQ_SCORE_GRAM_LAUNCHES) {
+      AWQ_TRY(launch_search_persistent(cfg.group_size, d, L, ws, Xt, Bm, hmax, Dbuf, W, absmax,
+                                       s_grid, inv_grid, partial, N, K, n_alpha, cfg.symmetric,
+                                       &persistent, st));
+    }
+  }
+  if (use_gram && !persistent) {
     AWQ_TRY(smem_attr(reinterpret_cast<const void*>(tri_gram), gram::SMEM_BYTES));
     AWQ_TRY(smem_attr(reinterpret_cast<const void*>(tri_score), gram::SMEM_BYTES));
     gp.K = static_cast<int>(K);
     gp.N = static_cast<int>(N);
-    gp.num_kb = nblk;  // TOK_BLOCK == BK: one k-block per token block
+    gp.num_kb = static_cast<int>(L.Tp / gram::BK);  // TOK_BLOCK == BK
     gp.num_tiles = gram_tiles(K);
     gp.B = Bm;
     gp.hmax = hmax;
@@ -829,9 +942,10 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     gp.num_kb = 0;
     gp.B = nullptr;
     ggrid = std::min(gp.num_tiles, std::min(d->sms, kPartialStride));
-  } else {
+  } else if (!use_gram) {
     AWQ_TRY(smem_attr(reinterpret_cast<const void*>(score::score_kernel), score::SMEM_BYTES));
   }
+  if (persistent) ggrid = d->sms;
   // 5. per alpha: residual D = W - Q(W diag s) diag(s)^-1, then its error score
   score::Params sp{};
   sp.tiles_n = static_cast<int>((N + score::BN - 1) / score::BN);
@@ -863,7 +977,9 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     cudaGetLastError();
     return AWQ_ERR_CUDA;
   };
-  if (use_gram) {
+  if (persistent) {
+    // the whole search ran in the persistent launch above
+  } else if (use_gram) {
     // every launch on the caller's stream: each scoring launch also builds the next residual
     for (int i = 0; i < n_alpha; ++i) {
       gp.D = Dbuf[i & 1];

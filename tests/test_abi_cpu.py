@@ -70,7 +70,7 @@ def test_score_mode_and_gram_workspace(L):
     finally:
         awq.awq_set_score_mode("auto")
     with pytest.raises(awq.AwqError):
-        awq.awq_set_score_mode(3)
+        awq.awq_set_score_mode(4)
     assert awq.awq_search_workspace_bytes(N, K, T, 20) == n
 
 

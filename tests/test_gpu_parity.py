@@ -283,6 +283,25 @@ def test_search_gram_deterministic_and_close_to_direct():
     assert bg == bd or abs(ed[bg] - ed[bd]) <= 1e-4 * ed[bd]
 
 
+@pytest.mark.parametrize("N,K,T,G", [(1000, 1024, 2048, 128), (700, 1664, 333, 128),
+                                     (130, 64, 1, 64), (4096, 512, 700, 64)])
+def test_search_gram_persistent_matches_launches(N, K, T, G):
+    """One persistent launch over H and every alpha (counters in global memory order its
+    phases) and one launch per phase give the same bits: the same tile deal per phase, the same
+    fixed-order partial sums."""
+    d = layer(N + 2 * K + T, N, K, T, n_out=max(1, K // 100))
+    W, X = dev(d["W"]), dev(d["X"])
+    alphas = synth.alpha_grid(20)
+    with score_mode("gram"):
+        a = awq.search_scale(W, X, alphas, G)
+        a2 = awq.search_scale(W, X, alphas, G)
+    with score_mode("gram_launches"):
+        b = awq.search_scale(W, X, alphas, G)
+    awq.awq_stream_status()
+    for u, v, w in zip(a, a2, b):
+        assert torch.equal(u, v) and torch.equal(u, w)
+
+
 def test_search_gram_zero_activations():
     """X = 0: H = 0, every error 0 and the first alpha wins."""
     d = layer(22, 256, 512, 300, n_out=4)
