@@ -218,6 +218,34 @@ awq_status_t awq_search_scale_static(const void* W_f16, int64_t N, int64_t K, co
                                      int32_t* best_idx, float* s_out, float* inv_s_out,
                                      awq_stream_t stream);
 
+/*
+ * Folding 1/s into the operation that produces the layer's input ("AWQ Math", "The equivalent
+ * transform": W' = W diag(s) on x' = diag(s)^-1 x gives the same output, so the quantised
+ * layer can run with inv_s = NULL once the previous operation emits x / s; "AWQ > Benefits and
+ * Practical Considerations": the scale folds into the previous layer).
+ *   A_f16 [rows, cols] fp16 row-major, row stride lda >= cols, modified in place:
+ *         A[r][c] = fp16_rne(fl32(A[r][c] * row_scale[r]))   (one IEEE fp32 multiply)
+ *   row_scale [rows] fp32 (pass inv_s).
+ * For the previous linear, A is its weight [C_out = K, C_in] (row k = output channel k); for a
+ * norm's weight vector, rows = K and cols = lda = 1.
+ */
+awq_status_t awq_scale_rows(void* A_f16, int64_t rows, int64_t cols, int64_t lda,
+                            const float* row_scale, awq_stream_t stream);
+
+/*
+ * The two elementwise operations of a Llama-style MLP block (RMSNorm -> gate/up -> SiLU(gate) *
+ * up -> down), for running the block end to end around the quantised linears. They are the
+ * block's own operations, not part of AWQ.
+ *   awq_rmsnorm:  Y[t][j] = fp16(X[t][j] * r_t * gamma[j]), r_t = 1 / sqrt(mean_j X[t][j]^2 +
+ *                 eps); X, Y [T, D] fp16 (D % 8 == 0), gamma [D] fp16; fp32 arithmetic, the
+ *                 sum of squares in a fixed order (deterministic).
+ *   awq_silu_mul: H[i] = fp16(silu(G[i]) * U[i]), silu(g) = g / (1 + e^-g); n % 8 == 0; fp32.
+ */
+awq_status_t awq_rmsnorm(const void* X_f16, int64_t T, int64_t D, const void* gamma_f16,
+                         float eps, void* Y_f16, awq_stream_t stream);
+awq_status_t awq_silu_mul(const void* G_f16, const void* U_f16, int64_t n, void* H_f16,
+                          awq_stream_t stream);
+
 /* Kernels of this library, as counted by the profiling calls below. */
 typedef enum {
   AWQ_K_CALIB_STATS = 0, /* awq_calib_stats (and the search when mean_abs is NULL) */
@@ -233,7 +261,10 @@ typedef enum {
   AWQ_K_GRAM = 10,       /* search, GRAM_LAUNCHES: tcgen05 lower triangle of H = X^T X, fp16 */
   AWQ_K_SCORE_GRAM = 11, /* search, GRAM_LAUNCHES: tcgen05 sum_n d_n^T H d_n of one alpha */
   AWQ_K_GRAM_SEARCH = 12, /* search, GRAM: persistent launch over H and every alpha */
-  AWQ_K_COUNT = 13
+  AWQ_K_SCALE_ROWS = 13,  /* awq_scale_rows */
+  AWQ_K_RMSNORM = 14,     /* awq_rmsnorm */
+  AWQ_K_SILU_MUL = 15,    /* awq_silu_mul */
+  AWQ_K_COUNT = 16
 } awq_kernel_id_t;
 
 /*

@@ -59,12 +59,17 @@ _SIGNATURES = {
     "awq_launch_count": (ctypes.c_uint64, []),
     "awq_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "awq_set_score_mode": (ctypes.c_int, [ctypes.c_int]),
+    "awq_scale_rows": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p]),
+    "awq_rmsnorm": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, ctypes.c_float, _c_void_p,
+                                   _c_void_p]),
+    "awq_silu_mul": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p]),
     "awq_profile_begin": (ctypes.c_int, []),
     "awq_profile_end": (ctypes.c_int, [_c_void_p, _c_void_p]),
 }
 
 KERNELS = ("calib_stats", "scale_grid", "absmax", "residual", "score", "finalize",
-           "quantize_pack", "gemv", "gemm_tc", "gram_prep", "gram", "score_gram", "gram_search")
+           "quantize_pack", "gemv", "gemm_tc", "gram_prep", "gram", "score_gram", "gram_search",
+           "scale_rows", "rmsnorm", "silu_mul")
 SCORE_MODES = {"auto": 0, "direct": 1, "gram": 2, "gram_launches": 3}
 
 _lib = None
@@ -163,6 +168,20 @@ def awq_w4a16_gemm(X, M, N, K, qweight, scales, zeros, inv_s, group_size, symmet
     _check("awq_w4a16_gemm", lib().awq_w4a16_gemm(
         _ptr(X), M, N, K, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s),
         _cfg(group_size, symmetric), _ptr(Y), _stream(stream)))
+
+
+def awq_scale_rows(A, rows, cols, lda, row_scale, stream=None):
+    _check("awq_scale_rows", lib().awq_scale_rows(_ptr(A), rows, cols, lda, _ptr(row_scale),
+                                                  _stream(stream)))
+
+
+def awq_rmsnorm(X, T, D, gamma, eps, Y, stream=None):
+    _check("awq_rmsnorm", lib().awq_rmsnorm(_ptr(X), T, D, _ptr(gamma), float(eps), _ptr(Y),
+                                            _stream(stream)))
+
+
+def awq_silu_mul(G, U, n, H, stream=None):
+    _check("awq_silu_mul", lib().awq_silu_mul(_ptr(G), _ptr(U), n, _ptr(H), _stream(stream)))
 
 
 def awq_status_string(status: int) -> str:

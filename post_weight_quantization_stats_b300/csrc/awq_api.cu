@@ -17,6 +17,7 @@
 
 #include "../../include/awq.h"
 #include "awq_device.cuh"
+#include "block_ops.cuh"
 #include "calib_stats.cuh"
 #include "gram_persistent.cuh"
 #include "gram_score.cuh"
@@ -733,6 +734,55 @@ awq_status_t awq_calib_stats(const void* X_f16, int64_t T, int64_t K, int64_t ld
   AWQ_TRY(device_info(&d));
   return launch_calib_stats(static_cast<const __half*>(X_f16), T, K, ldx, mean_abs,
                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+awq_status_t awq_scale_rows(void* A_f16, int64_t rows, int64_t cols, int64_t lda,
+                           const float* row_scale, awq_stream_t stream) {
+  if (!A_f16 || !row_scale || rows < 1 || cols < 1 || lda < cols) return AWQ_ERR_INVALID_ARG;
+  if (rows * lda > kMaxElems) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A_f16) || !aligned4(row_scale)) return AWQ_ERR_MISALIGNED;
+  DeviceInfo* d = nullptr;
+  AWQ_TRY(device_info(&d));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int vec8 = (cols % 8 == 0 && lda % 8 == 0) ? 1 : 0;
+  const long long work = vec8 ? rows * (cols / 8) : rows * cols;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(4LL * d->sms, (work + 255) / 256));
+  prof_start(AWQ_K_SCALE_ROWS, st);
+  block::scale_rows_kernel<<<grid, 256, 0, st>>>(static_cast<__half*>(A_f16), rows, cols, lda,
+                                                 row_scale, vec8);
+  return launched(AWQ_K_SCALE_ROWS, st);
+}
+
+awq_status_t awq_rmsnorm(const void* X_f16, int64_t T, int64_t D, const void* gamma_f16,
+                         float eps, void* Y_f16, awq_stream_t stream) {
+  if (!X_f16 || !gamma_f16 || !Y_f16 || T < 1 || D < 1 || !(eps >= 0.0f))
+    return AWQ_ERR_INVALID_ARG;
+  if (D % 8 != 0 || T * D > kMaxElems || T > 0x7fffffffLL) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(X_f16) || !aligned16(gamma_f16) || !aligned16(Y_f16)) return AWQ_ERR_MISALIGNED;
+  DeviceInfo* d = nullptr;
+  AWQ_TRY(device_info(&d));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  prof_start(AWQ_K_RMSNORM, st);
+  block::rmsnorm_kernel<<<static_cast<unsigned>(T), 256, 0, st>>>(
+      static_cast<const __half*>(X_f16), static_cast<int>(D),
+      static_cast<const __half*>(gamma_f16), eps, static_cast<__half*>(Y_f16));
+  return launched(AWQ_K_RMSNORM, st);
+}
+
+awq_status_t awq_silu_mul(const void* G_f16, const void* U_f16, int64_t n, void* H_f16,
+                          awq_stream_t stream) {
+  if (!G_f16 || !U_f16 || !H_f16 || n < 1) return AWQ_ERR_INVALID_ARG;
+  if (n % 8 != 0 || n > kMaxElems) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(G_f16) || !aligned16(U_f16) || !aligned16(H_f16)) return AWQ_ERR_MISALIGNED;
+  DeviceInfo* d = nullptr;
+  AWQ_TRY(device_info(&d));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(4LL * d->sms, (n / 8 + 255) / 256));
+  prof_start(AWQ_K_SILU_MUL, st);
+  block::silu_mul_kernel<<<grid, 256, 0, st>>>(static_cast<const __half*>(G_f16),
+                                               static_cast<const __half*>(U_f16), n,
+                                               static_cast<__half*>(H_f16));
+  return launched(AWQ_K_SILU_MUL, st);
 }
 
 awq_status_t awq_quantize_pack(const void* W_f16, int64_t N, int64_t K, const float* s,
