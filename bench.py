@@ -743,33 +743,61 @@ def kernel_rooflines(prof, alg, peaks, bench_workload):
 
 
 def e2e_run(awq, torch, step, layer, args, world):
-    """The same step through the public API from pinned host buffers: H2D of W and X, the step,
-    D2H of every result, all inside the timed region."""
+    """The same step through the public API from pinned host buffers, every step's H2D of W and
+    X and D2H of every result inside the timed region. Two sets of device buffers alternate and
+    the copies run on their own streams (one per direction), so the upload of step i+1 and the
+    download of step i-1 overlap the computation of step i, as a layer-by-layer quantisation
+    pipeline would run; each buffer set is reused only after its previous step's results have
+    been read back."""
     W_h = torch.from_numpy(layer["W"]).pin_memory()
     X_h = torch.from_numpy(layer["X"]).pin_memory()
-    outs = step.outputs()
-    hosts = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    wl, _ = layer_units(args.workload)
+    bufs = [step, LayerStep(awq, torch, layer, wl, step.W.device)]
+    hosts = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in b.outputs()] for b in bufs]
     h2d = W_h.numel() * 2 + X_h.numel() * 2
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    d2h = sum(o.numel() * o.element_size() for o in step.outputs())
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    uploaded = [ev(), ev()]
+    computed = [ev(), ev()]
+    read_back = [ev(), ev()]
+    used = [False, False]
 
-    def one():
-        step.W.copy_(W_h, non_blocking=True)
-        step.X.copy_(X_h, non_blocking=True)
-        step.enqueue()
-        for h, o in zip(hosts, outs):
-            h.copy_(o, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+    def one(i):
+        k = i % 2
+        b = bufs[k]
+        with torch.cuda.stream(up):
+            if used[k]:
+                up.wait_event(computed[k])          # the step before last has read W and X
+            b.W.copy_(W_h, non_blocking=True)
+            b.X.copy_(X_h, non_blocking=True)
+            uploaded[k].record(up)
+        comp.wait_event(uploaded[k])
+        if used[k]:
+            comp.wait_event(read_back[k])           # its results have been read back
+        b.enqueue()
+        computed[k].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[k])
+            for h, o in zip(hosts[k], b.outputs()):
+                h.copy_(o, non_blocking=True)
+            read_back[k].record(down)
+        used[k] = True
 
-    for _ in range(max(1, args.warmup)):
-        one()
+    for i in range(max(2, args.warmup)):
+        one(i)
+    torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        one()
+    for i in range(args.steps):
+        one(i)
+    torch.cuda.synchronize()
     dt = max_over_ranks(time.perf_counter() - t0, world)
     return {"value": world * args.steps / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "pipelining": "two buffer sets; H2D and D2H on their own streams overlap compute"}
 
 
 def run_case(args):
