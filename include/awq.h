@@ -187,7 +187,11 @@ uint64_t awq_launch_count(void);
 
 /*
  * Limit, in nanoseconds, of every bounded device-side wait in later launches (default 2e9).
- * Returns the previous value.
+ * Returns the previous value. A kernel that gives up records AWQ_ERR_TIMEOUT (see
+ * awq_stream_status); its outputs are then undefined, the context stays usable. The waits by
+ * which a giving-up CTA lets its own copies and MMAs in flight finish before it exits keep a
+ * floor of 0.5 s, so even 0 exercises the give-up path safely: with 0 a wait that is not
+ * already met gives up at once (in practice every pipelined kernel then reports a timeout).
  */
 uint64_t awq_set_wait_limit_ns(uint64_t limit_ns);
 

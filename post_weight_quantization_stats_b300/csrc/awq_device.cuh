@@ -61,6 +61,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking check of the same phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Everything a bounded wait needs: the limit, a CTA-wide abort flag (shared memory) and the
 // device status word (global memory).
 struct WaitCtx {
@@ -74,6 +87,12 @@ struct WaitCtx {
 // CTA's abort flag and records AWQ_ERR_TIMEOUT in the device status word.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   const uint32_t a = smem_u32(bar);
+  if (w.limit_ns == 0) {  // a limit of 0 never waits: exercises the give-up path on demand
+    if (mbar_test_wait(a, parity)) return true;
+    *w.abort_flag = 1;
+    atomicCAS(w.status, 0, kStatusTimeout);
+    return false;
+  }
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -90,12 +109,17 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
 }
 
 // Same, ignoring the abort flag: used on the way out to let copies/MMAs already in flight land.
+// Its limit is at least kDrainFloorNs whatever the configured wait limit, so a short limit (even
+// 0, which makes every other wait give up at once) never lets a CTA exit while its own copies
+// into shared memory or MMAs into TMEM are still running.
+constexpr uint64_t kDrainFloorNs = 500000000ull;
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
+  const uint64_t lim = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(a, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (globaltimer_ns() - t0 > lim) return false;
   }
 }
 

@@ -67,6 +67,11 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ bool wait_count(const unsigned int* c, unsigned int target,
                                            const WaitCtx& w) {
   if (ld_acquire_gpu(c) >= target) return true;
+  if (w.limit_ns == 0) {  // never waits (see wait_bounded)
+    *w.abort_flag = 1;
+    atomicCAS(w.status, 0, kStatusTimeout);
+    return false;
+  }
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     __nanosleep(100);
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (!ok) {  // let the copies already issued land before the CTA exits
+      {  // let the copies issued last land before the CTA exits (at once unless it gave up)
         const uint32_t first = it > STAGES ? it - STAGES : 0u;
         for (uint32_t j = first; j < it; ++j)
           wait_drain(&full[j % STAGES], (j / STAGES) & 1u, p.limit_ns);

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kb * BK, t.rb * BN);
         }
       }
-      if (!ok) {  // let the copies already issued land before the CTA exits
+      {  // let the copies issued last land before the CTA exits (at once unless it gave up)
         const uint32_t first = it > STAGES ? it - STAGES : 0u;
         for (uint32_t j = first; j < it; ++j)
           wait_drain(&full[j % STAGES], (j / STAGES) & 1u, p.limit_ns);

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         tma_load_2d(st + XRAW_OFF, &tmX, &full_raw[s], k0, 0);
         if (a.inv_s) bulk_load_plain(st + INV_OFF, a.inv_s + k0, inv_bytes, &full_raw[s]);
       }
-      if (!ok) {
+      {  // let the copies issued last land before the CTA exits (at once unless it gave up)
         for (int jj = (j > RAW_STAGES ? j - RAW_STAGES : 0); jj < j; ++jj)
           wait_drain(&full_raw[jj % RAW_STAGES], (jj / RAW_STAGES) & 1u, a.limit_ns);
       }
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           bulk_load_plain(st + C::B_BYTES + CODES_BYTES, a.inv_s + k0,
                           static_cast<uint32_t>(klen) * 4u, &full_raw[s]);
       }
-      if (!ok) {
+      {  // let the copies issued last land before the CTA exits (at once unless it gave up)
         for (int jj = (j > C::RAW_STAGES ? j - C::RAW_STAGES : 0); jj < j; ++jj)
           wait_drain(&full_raw[jj % C::RAW_STAGES], (jj / C::RAW_STAGES) & 1u, a.limit_ns);
       }

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
         bulk_load(ring + static_cast<size_t>(s) * a.stage_bytes,
                   a.Q + static_cast<long long>(row_lo) * (a.K >> 3), bytes, &full[s], pol);
       }
-      if (!ok) {  // gave up: let the copies already issued land before the CTA exits
+      {  // let the copies issued last land before the CTA exits (at once unless it gave up)
         for (int jj = (j > a.nstages ? j - a.nstages : 0); jj < j; ++jj)
           wait_drain(&full[jj % a.nstages], (jj / a.nstages) & 1u, a.limit_ns);
       }

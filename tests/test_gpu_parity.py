@@ -420,3 +420,55 @@ def test_w4a16_deterministic():
         a = awq.w4a16_gemm(X[:M].contiguous(), q, sc, z)
         b = awq.w4a16_gemm(X[:M].contiguous(), q, sc, z)
         assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------------------- bounded waits
+
+def test_bounded_waits_give_up_and_recover():
+    """With the wait limit at 0 every pipelined kernel gives up at its first unmet wait: the
+    call reports AWQ_ERR_TIMEOUT through awq_stream_status (no hang, no fault). With the limit
+    restored the same calls give the same bits as before. Covers the persistent Gram search
+    (cross-CTA counters), the one-launch-per-phase Gram kernels, the direct scoring kernel and
+    the decode GEMV."""
+    d = layer(31, 512, 1024, 1500, n_out=8)
+    W, X = dev(d["W"]), dev(d["X"])
+    alphas = synth.alpha_grid(8)
+    qd = ref.quantize_pack(d["W"], None)
+    q, sc, z = dev(qd["qweight"].view(np.int32)), dev(qd["scales"]), dev(qd["zeros"])
+    xg = dev(d["X"][:1])
+
+    def run_all():
+        outs = []
+        for mode in ("gram", "gram_launches", "direct"):
+            with score_mode(mode):
+                outs.append(awq.search_scale(W, X, alphas))
+        outs.append((awq.w4a16_gemm(xg, q, sc, z),))
+        return outs
+
+    want = run_all()
+    awq.awq_stream_status()
+    old = awq.awq_set_wait_limit_ns(0)
+    timeouts = 0
+    try:
+        for mode in ("gram", "gram_launches", "direct"):
+            with score_mode(mode):
+                awq.search_scale(W, X, alphas)
+            try:
+                awq.awq_stream_status()
+            except awq.AwqError as e:
+                assert e.name == "AWQ_ERR_TIMEOUT", e
+                timeouts += 1
+        awq.w4a16_gemm(xg, q, sc, z)
+        try:
+            awq.awq_stream_status()
+        except awq.AwqError as e:
+            assert e.name == "AWQ_ERR_TIMEOUT", e
+            timeouts += 1
+    finally:
+        awq.awq_set_wait_limit_ns(old)
+    assert timeouts >= 3, timeouts
+    got = run_all()
+    awq.awq_stream_status()
+    for a, b in zip(want, got):
+        for u, v in zip(a, b):
+            assert torch.equal(u, v)
