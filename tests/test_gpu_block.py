@@ -144,3 +144,42 @@ def test_awq_mlp_stack_end_to_end():
     e_awq = torch.mean((y_awq - y_fp) ** 2).item()
     e_rtn = torch.mean((y_rtn - y_fp) ** 2).item()
     assert e_awq < e_rtn, (e_awq, e_rtn)
+
+
+def test_stack_run_resumes_bit_identically(tmp_path):
+    """Three linears through the resumable stack run on the GPU quantiser: stopped after the
+    second, restarted, the results equal an uninterrupted run's bit for bit, and the first
+    layer's alpha equals the oracle's search on the same statistic."""
+    from post_weight_quantization_stats_b300 import stack
+
+    def layers():
+        out = []
+        for i in range(3):
+            d = synth.random_layer(40 + i, 256, 512, 300, n_out=5)
+            out.append((i, f"l{i}", lambda d=d: (dev(d["W"]), dev(d["X"]))))
+        return out
+
+    alphas = synth.alpha_grid(20)
+    q = stack.gpu_quantizer(alphas)
+    clean = str(tmp_path / "clean")
+    want = stack.quantize_layers(layers(), clean, q)
+
+    class Stop(Exception):
+        pass
+
+    def stop(i):
+        if i == 1:
+            raise Stop()
+    d = str(tmp_path / "run")
+    with pytest.raises(Stop):
+        stack.quantize_layers(layers(), d, q, on_layer=stop)
+    got = stack.quantize_layers(layers(), d, q)
+    assert sorted(got) == [0, 1, 2]
+    for i in range(3):
+        a, b = stack.load_layer(clean, want[i]), stack.load_layer(d, got[i])
+        for k in a:
+            assert np.array_equal(a[k], b[k]), (i, k)
+    l0 = synth.random_layer(40, 256, 512, 300, n_out=5)
+    r = ref.search_scale(l0["W"], l0["X"], alphas, m=stack.load_layer(d, got[0])["m"])
+    b = int(stack.load_layer(d, got[0])["best"])
+    assert b == r["best"] or r["err"][b] <= r["err"][r["best"]] * (1 + 1e-4)
