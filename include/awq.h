@@ -41,7 +41,7 @@
  *     an error code and enqueues nothing. Kernel launch failures return AWQ_ERR_CUDA.
  *   - The pipelined tensor-core kernels bound every wait; a kernel that gives up records
  *     AWQ_ERR_TIMEOUT in a device status word that awq_stream_status reports.
- *   - Shapes: G (group size) is 64 or 128, K % G == 0, all sizes >= 1, and N * K, T * K and
+ *   - Shapes: G (group size) is 32, 64 or 128, K % G == 0, all sizes >= 1, and N * K, T * K and
  *     M * max(N, K) below 2^31 elements.
  */
 #ifndef AWQ_H_
@@ -69,7 +69,7 @@ typedef enum {
 } awq_status_t;
 
 typedef struct {
-  int32_t group_size; /* 64 or 128 input channels per (step, zero point) */
+  int32_t group_size; /* 32, 64 or 128 input channels per (step, zero point) */
   int32_t symmetric;  /* 0: asymmetric with zero point; 1: step = max|w| / 8, zero point 8 */
 } awq_qcfg_t;
 
@@ -94,7 +94,8 @@ awq_status_t awq_calib_stats(const void* X_f16, int64_t T, int64_t K, int64_t ld
  *   GRAM_LAUNCHES  the same arithmetic with one launch for H and one per candidate (same
  *           results, bit for bit).
  *   AUTO    GRAM when it takes fewer tensor-core steps (long calibration sets, T > K / 2 or
- *           so), the workspace holds it, and K T, K K < 2^31; DIRECT otherwise.
+ *           so), the workspace holds it, K % 64 == 0 and K T, K K < 2^31; DIRECT otherwise.
+ *           Forcing GRAM on another shape returns AWQ_ERR_UNSUPPORTED_SHAPE.
  * Returns AWQ_ERR_INVALID_ARG for any other value.
  */
 typedef enum {

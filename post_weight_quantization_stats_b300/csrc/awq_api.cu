@@ -114,7 +114,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 awq_status_t check_cfg(awq_qcfg_t cfg) {
-  if (cfg.group_size != 64 && cfg.group_size != 128) return AWQ_ERR_INVALID_ARG;
+  if (cfg.group_size != 32 && cfg.group_size != 64 && cfg.group_size != 128)
+    return AWQ_ERR_INVALID_ARG;
   if (cfg.symmetric != 0 && cfg.symmetric != 1) return AWQ_ERR_INVALID_ARG;
   return AWQ_OK;
 }
@@ -266,8 +267,10 @@ awq_status_t launch_quantize_pack(const __half* W, int64_t N, int64_t K, const f
   prof_start(AWQ_K_QUANTIZE_PACK, st);
   if (cfg.group_size == 128)
     quantize_pack_kernel<128><<<grid, 256, 0, st>>>(a);
-  else
+  else if (cfg.group_size == 64)
     quantize_pack_kernel<64><<<grid, 256, 0, st>>>(a);
+  else
+    quantize_pack_kernel<32><<<grid, 256, 0, st>>>(a);
   return launched(AWQ_K_QUANTIZE_PACK, st);
 }
 
@@ -328,7 +331,8 @@ awq_status_t launch_w4_dequant_bn(const __half* X, const w4tc::Args& a0, int G, 
   AWQ_TRY(make_map_plain(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a.Q, a.N, a.K / 8, a.K / 8,
                          dk::BK / 8, w4tc::BM));
   AWQ_TRY(make_map(&mx, X, a.M, a.K, a.K, BN));
-  auto kern = G == 128 ? dk::dequant_kernel<BN, 128> : dk::dequant_kernel<BN, 64>;
+  auto kern = G == 128 ? dk::dequant_kernel<BN, 128>
+              : G == 64 ? dk::dequant_kernel<BN, 64> : dk::dequant_kernel<BN, 32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) {
     cudaGetLastError();
     return AWQ_ERR_CUDA;
@@ -376,7 +380,8 @@ awq_status_t gemv_shape(gemv::Args& a, int G, int sms) {
 template <int M>
 awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
   const size_t smem = gemv::smem_bytes(a);
-  auto kern = (G == 128) ? gemv::gemv_kernel<M, 128> : gemv::gemv_kernel<M, 64>;
+  auto kern = G == 128 ? gemv::gemv_kernel<M, 128>
+              : G == 64 ? gemv::gemv_kernel<M, 64> : gemv::gemv_kernel<M, 32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
@@ -500,11 +505,13 @@ SearchLayout search_layout(int64_t N, int64_t K, int64_t T, int32_t n_alpha) {
   return L;
 }
 
-// Shapes the Gram schedule handles: 32-bit element offsets for X^T and H, a transpose grid
-// within the launch limits.
+// Shapes the Gram schedule handles: K a multiple of 64 (the transpose's channel blocks and the
+// triangle's epilogue work in 64- and 32-channel pieces), 32-bit element offsets for X^T and H,
+// a transpose grid within the launch limits.
 bool gram_shape_ok(int64_t K, int64_t T) {
   const int64_t Tp = (T + gram::TOK_BLOCK - 1) / gram::TOK_BLOCK * gram::TOK_BLOCK;
-  return K * Tp <= kMaxElems && K * K <= kMaxElems && Tp / gram::TOK_BLOCK <= 65535;
+  return K % 64 == 0 && K * Tp <= kMaxElems && K * K <= kMaxElems &&
+         Tp / gram::TOK_BLOCK <= 65535;
 }
 
 // Tile counts of the Gram schedule's two kernel modes.
@@ -606,7 +613,8 @@ awq_status_t launch_search_persistent(int G, DeviceInfo* d, const SearchLayout& 
   sp.sync = reinterpret_cast<unsigned int*>(ws + L.sync);
   sp.status = d->status;
   sp.limit_ns = g_wait_limit_ns.load();
-  auto kern = G == 128 ? gram::search_kernel<128> : gram::search_kernel<64>;
+  auto kern = G == 128 ? gram::search_kernel<128>
+              : G == 64 ? gram::search_kernel<64> : gram::search_kernel<32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gram::SMEM_BYTES) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -940,9 +948,11 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   bool persistent = false;
   using TriKern = void (*)(CUtensorMap, CUtensorMap, gram::Params);
   const TriKern tri_gram = cfg.group_size == 128 ? gram::tri_kernel<gram::GRAM, 128>
-                                                 : gram::tri_kernel<gram::GRAM, 64>;
+                           : cfg.group_size == 64 ? gram::tri_kernel<gram::GRAM, 64>
+                                                  : gram::tri_kernel<gram::GRAM, 32>;
   const TriKern tri_score = cfg.group_size == 128 ? gram::tri_kernel<gram::SCORE, 128>
-                                                  : gram::tri_kernel<gram::SCORE, 64>;
+                            : cfg.group_size == 64 ? gram::tri_kernel<gram::SCORE, 64>
+                                                   : gram::tri_kernel<gram::SCORE, 32>;
   // the residual of candidate i into buffer i % 2
   auto res_args = [&](int i) {
     return ResidualArgs{W, s_grid + static_cast<size_t>(i) * K, inv_grid + static_cast<size_t>(i) * K,
@@ -1018,8 +1028,10 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     prof_start(AWQ_K_RESIDUAL, rs);
     if (cfg.group_size == 128)
       residual_kernel<128><<<rgrid, 256, 0, rs>>>(ra);
-    else
+    else if (cfg.group_size == 64)
       residual_kernel<64><<<rgrid, 256, 0, rs>>>(ra);
+    else
+      residual_kernel<32><<<rgrid, 256, 0, rs>>>(ra);
     return launched(AWQ_K_RESIDUAL, rs);
   };
   auto ev = [](cudaError_t e) -> awq_status_t {
@@ -1121,7 +1133,9 @@ awq_status_t awq_w4a16_gemm(const void* X_f16, int64_t M, int64_t N, int64_t K,
   a.status = d->status;
   a.limit_ns = g_wait_limit_ns.load();
   const __half* X = static_cast<const __half*>(X_f16);
-  if (M <= w4tc::grouped::BN) return launch_w4_grouped(X, a, G, d->sms, st);
+  // the grouped kernel gives every group of 64 or more channels its own accumulator; G = 32
+  // takes the dequant kernel at every M above the GEMV's
+  if (M <= w4tc::grouped::BN && G >= 64) return launch_w4_grouped(X, a, G, d->sms, st);
   return launch_w4_dequant(X, a, G, d->sms, st);
 }
 

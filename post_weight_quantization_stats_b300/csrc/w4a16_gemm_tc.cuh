@@ -587,22 +587,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool row_ok = row < a.N;
     bool ok = true;
     // group parameters of stage j, loaded PD stages ahead and kept as loaded (fp16, uint8)
-    // until used, so the loads stay in flight
+    // until used, so the loads stay in flight; a 64-channel half holds one group, or two when
+    // G = 32 (NG sets per stage)
     constexpr int PD = 4;
-    auto load_params = [&](int j, __half& st, uint8_t& z) {
+    constexpr int NG = G >= 64 ? 1 : 64 / G;
+    auto load_params = [&](int j, __half (&st)[NG], uint8_t (&z)[NG]) {
       const int k = (kb_lo + j) * BK + h * 64;
-      if (row_ok && j < nst && k < a.K) {
-        const long long gi = static_cast<long long>(k / G) * a.N + row;
-        st = a.scales[gi];
-        if (a.zeros) z = a.zeros[gi];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        if (row_ok && j < nst && k + g * G < a.K) {
+          const long long gi = static_cast<long long>((k + g * G) / G) * a.N + row;
+          st[g] = a.scales[gi];
+          if (a.zeros) z[g] = a.zeros[gi];
+        }
       }
     };
-    __half pst[PD];
-    uint8_t pz[PD];
+    __half pst[PD][NG];
+    uint8_t pz[PD][NG];
 #pragma unroll
     for (int u = 0; u < PD; ++u) {
-      pst[u] = __float2half_rn(0.f);
-      pz[u] = 8;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        pst[u][g] = __float2half_rn(0.f);
+        pz[u][g] = 8;
+      }
       load_params(u, pst[u], pz[u]);
     }
     for (int j0 = 0; j0 < nst; j0 += PD) {
@@ -610,7 +618,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int u = 0; u < PD; ++u) {
       const int j = j0 + u;
       if (j >= nst) break;
-      const float st_cur = __half2float(pst[u]), z_cur = static_cast<float>(pz[u]);
+      float st_cur[NG], z_cur[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        st_cur[g] = __half2float(pst[u][g]);
+        z_cur[g] = static_cast<float>(pz[u][g]);
+      }
       load_params(j + PD, pst[u], pz[u]);
       const int s = j % C::RAW_STAGES, sab = j % AB_STAGES;
       if (ok) ok = wait_bounded(&full_raw[s], (j / C::RAW_STAGES) & 1u, wc);
@@ -629,14 +642,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint4 q0 = *reinterpret_cast<const uint4*>(st + C::B_BYTES + r * 64 + h * 32);
           const uint4 q1 = *reinterpret_cast<const uint4*>(st + C::B_BYTES + r * 64 + h * 32 + 16);
           const uint32_t wq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          const __half2 zlo = __float2half2_rn(-(1024.f + z_cur));
-          const __half2 zhi = __float2half2_rn(-(64.f + z_cur));
-          const __half2 st2 = __float2half2_rn(st_cur);
           const float* inv = reinterpret_cast<const float*>(st + C::B_BYTES + CODES_BYTES) + h * 64;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 v = a.inv_s ? dequant8_inv(wq[c], zlo, zhi, st2, inv + 8 * c)
-                                    : dequant8_f16(wq[c], zlo, zhi, st2);
+            const int g = (c * 8) / (64 / NG);   // the group of words c (8 channels each)
+            const __half2 zlo = __float2half2_rn(-(1024.f + z_cur[g]));
+            const __half2 zhi = __float2half2_rn(-(64.f + z_cur[g]));
+            const __half2 st2 = __float2half2_rn(st_cur[g]);
+            uint4 v = a.inv_s ? dequant8_inv(wq[c], zlo, zhi, st2, inv + 8 * c)
+                              : dequant8_f16(wq[c], zlo, zhi, st2);
+            // channels past K (K % 128 == 32 or 96 with G = 32): their codes and inv_s slots
+            // hold fill or stale data, so the weights are zeroed rather than trusted
+            if (kbase + 8 * c >= a.K) v = make_uint4(0u, 0u, 0u, 0u);
             av[4 * c + 0] = v.x;
             av[4 * c + 1] = v.y;
             av[4 * c + 2] = v.z;

@@ -71,6 +71,19 @@ def test_score_mode_and_gram_workspace(L):
         awq.awq_set_score_mode("auto")
     with pytest.raises(awq.AwqError):
         awq.awq_set_score_mode(4)
+    # GRAM needs K % 64 == 0: forced on K = 800 (G = 32) it is refused before any launch
+    A = 1 << 20
+    alphas = (ctypes.c_float * 2)(0.0, 0.5)
+    cfg = awq.QCfg(32, 0)
+    awq.awq_set_score_mode("gram")
+    try:
+        assert awq.awq_search_workspace_bytes(64, 800, 256, 2, group_size=32) == 0
+        assert L.awq_search_scale(A, 64, 800, A, 256, None, ctypes.cast(alphas, ctypes.c_void_p),
+                                  2, cfg, A, 1 << 30, A, A, None, None, None) == \
+            awq.STATUS_CODE["AWQ_ERR_UNSUPPORTED_SHAPE"]
+    finally:
+        awq.awq_set_score_mode("auto")
+    assert awq.awq_search_workspace_bytes(64, 800, 256, 2, group_size=32) > 0
     assert awq.awq_search_workspace_bytes(N, K, T, 20) == n
 
 
@@ -89,7 +102,7 @@ def test_host_validation_rejects_without_cuda(L):
     assert _code(L, "awq_calib_stats", A + 2, 8, 128, 128, A, None) == S["AWQ_ERR_MISALIGNED"]
     assert _code(L, "awq_quantize_pack", A, 16, 100, None, cfg, A, A, A, None) == \
         S["AWQ_ERR_UNSUPPORTED_SHAPE"]
-    assert _code(L, "awq_quantize_pack", A, 16, 256, None, awq.QCfg(32, 0), A, A, A, None) == \
+    assert _code(L, "awq_quantize_pack", A, 16, 256, None, awq.QCfg(48, 0), A, A, A, None) == \
         S["AWQ_ERR_INVALID_ARG"]
     assert _code(L, "awq_quantize_pack", A, 16, 256, None, cfg, A, A, None, None) == \
         S["AWQ_ERR_INVALID_ARG"]                          # asymmetric needs zeros

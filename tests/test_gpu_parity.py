@@ -71,7 +71,7 @@ QP_SHAPES = [(512, 512), (300, 1152), (1, 128), (7, 64), (33, 4096)]
 
 
 @pytest.mark.parametrize("N,K", QP_SHAPES)
-@pytest.mark.parametrize("G", [64, 128])
+@pytest.mark.parametrize("G", [32, 64, 128])
 @pytest.mark.parametrize("sym", [False, True])
 @pytest.mark.parametrize("with_s", [False, True])
 def test_quantize_pack_bitexact(N, K, G, sym, with_s):
@@ -212,7 +212,8 @@ def test_search_tiny_layer():
 
 @pytest.mark.parametrize("N,K,T,G,sym", [(300, 384, 100, 128, False), (256, 512, 129, 64, False),
                                          (512, 512, 64, 128, True), (1, 128, 1, 128, False),
-                                         (17, 256, 300, 64, True)])
+                                         (17, 256, 300, 64, True), (200, 352, 150, 32, False),
+                                         (64, 96, 40, 32, True)])
 def test_search_ragged(N, K, T, G, sym):
     d = layer(N + K + T, N, K, T, n_out=max(1, K // 100))
     _check_search(d["W"], d["X"], synth.alpha_grid(20), G, sym, use_m=True)
@@ -250,7 +251,7 @@ def test_search_overlapped_schedule_matches_serial():
         assert torch.equal(u, v)
 
 
-GRAM_CASES = [(700, 1664, 333, 128, False), (256, 512, 4000, 64, False),
+GRAM_CASES = [(700, 1664, 333, 128, False), (256, 512, 4000, 64, False), (300, 832, 900, 32, False),
               (1000, 1024, 2048, 128, True), (130, 64, 1, 64, False), (33, 4096, 700, 128, False),
               (129, 320, 64, 64, True)]
 
@@ -379,11 +380,21 @@ def test_w4a16_batch_sizes(M):
 @pytest.mark.parametrize("N,K", [(512, 512), (300, 1152), (1, 128), (130, 64), (4096, 4096)])
 @pytest.mark.parametrize("M", [1, 8, 16, 128])
 @pytest.mark.parametrize("G,sym,with_inv", [(128, False, False), (64, False, True),
-                                            (128, True, True), (64, True, False)])
+                                            (128, True, True), (64, True, False),
+                                            (32, False, True), (32, True, False)])
 def test_w4a16_shapes(N, K, M, G, sym, with_inv):
     if K % G:
         pytest.skip("K % G")
     _gemm_case(N, K, M, G, sym, with_inv, N * 7 + K + M)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 16, 17, 200])
+def test_w4a16_group_32(M):
+    """G = 32: two groups per 64-channel expander half in the dequant kernel (the grouped kernel
+    needs G >= 64, so every M above the GEMV's takes the dequant kernel); K = 1568 ends 32
+    channels into a 128-channel stage."""
+    _gemm_case(520, 1536, M, 32, False, True, 300 + M)
+    _gemm_case(200, 1568, M, 32, True, True, 400 + M)
 
 
 def test_w4a16_large_k_chunked_gemv():
