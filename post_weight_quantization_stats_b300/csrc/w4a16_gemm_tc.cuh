@@ -643,21 +643,34 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint4 q1 = *reinterpret_cast<const uint4*>(st + C::B_BYTES + r * 64 + h * 32 + 16);
           const uint32_t wq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
           const float* inv = reinterpret_cast<const float*>(st + C::B_BYTES + CODES_BYTES) + h * 64;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int g = (c * 8) / (64 / NG);   // the group of words c (8 channels each)
+          auto expand = [&](int c) -> uint4 {
+            const int g = (c * 8) / (64 / NG);   // the group of word c (8 channels)
             const __half2 zlo = __float2half2_rn(-(1024.f + z_cur[g]));
             const __half2 zhi = __float2half2_rn(-(64.f + z_cur[g]));
             const __half2 st2 = __float2half2_rn(st_cur[g]);
-            uint4 v = a.inv_s ? dequant8_inv(wq[c], zlo, zhi, st2, inv + 8 * c)
-                              : dequant8_f16(wq[c], zlo, zhi, st2);
-            // channels past K (K % 128 == 32 or 96 with G = 32): their codes and inv_s slots
-            // hold fill or stale data, so the weights are zeroed rather than trusted
-            if (kbase + 8 * c >= a.K) v = make_uint4(0u, 0u, 0u, 0u);
-            av[4 * c + 0] = v.x;
-            av[4 * c + 1] = v.y;
-            av[4 * c + 2] = v.z;
-            av[4 * c + 3] = v.w;
+            return a.inv_s ? dequant8_inv(wq[c], zlo, zhi, st2, inv + 8 * c)
+                           : dequant8_f16(wq[c], zlo, zhi, st2);
+          };
+          if (kbase + 64 <= a.K) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = expand(c);
+              av[4 * c + 0] = v.x;
+              av[4 * c + 1] = v.y;
+              av[4 * c + 2] = v.z;
+              av[4 * c + 3] = v.w;
+            }
+          } else {
+            // the half reaches past K (K % 128 == 32 or 96, G = 32): the codes and inv_s slots
+            // of channels past K hold fill or stale data, so their weights are zeroed
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = kbase + 8 * c < a.K ? expand(c) : make_uint4(0u, 0u, 0u, 0u);
+              av[4 * c + 0] = v.x;
+              av[4 * c + 1] = v.y;
+              av[4 * c + 2] = v.z;
+              av[4 * c + 3] = v.w;
+            }
           }
         }
         tmem_st_x32(tmem_base + a_lane + static_cast<uint32_t>(C::A_COL0 + sab * A_COLS + h * 32), av);
