@@ -143,8 +143,9 @@ size_t awq_search_workspace_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alp
  * together with the events that order it); it forks from `stream` and rejoins it before the
  * call's last kernel, so the whole sequence can be captured in a CUDA graph once that first
  * call has been made. Searches issued concurrently on one device serialise their residual
- * kernels on that stream. The GRAM and SERIAL schedules use `stream` alone (GRAM builds each
- * next residual inside the scoring launch).
+ * kernels on that stream. GRAM uses that stream only for the scale grid and max|W|, which run
+ * beside the transpose of X (same fork and join); it builds each next residual inside the
+ * scoring launch. SERIAL uses `stream` alone.
  */
 awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
                               int64_t T, const float* mean_abs, const float* alphas,

@@ -914,6 +914,16 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     AWQ_TRY(launch_calib_stats(X, T, K, K, m, st));
     mp = m;
   }
+  // GRAM: the scale grid and max|W| (steps 2-3) run on the library's second stream while X^T
+  // and its column sums are formed on the caller's (step 4); they join before the search
+  cudaStream_t ps = st;
+  if (use_gram) {
+    if (cudaEventRecord(d->fork, st) != cudaSuccess || cudaStreamWaitEvent(d->side, d->fork, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return AWQ_ERR_CUDA;
+    }
+    ps = d->side;
+  }
   // 2. scale grid
   GridArgs ga{};
   ga.m = mp;
@@ -922,19 +932,19 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   ga.K = static_cast<int>(K);
   ga.n_alpha = n_alpha;
   for (int i = 0; i < n_alpha; ++i) ga.alphas[i] = alphas[i];
-  prof_start(AWQ_K_SCALE_GRID, st);
-  scale_grid_kernel<<<static_cast<unsigned>((K * n_alpha + 255) / 256), 256, 0, st>>>(ga);
-  AWQ_TRY(launched(AWQ_K_SCALE_GRID, st));
+  prof_start(AWQ_K_SCALE_GRID, ps);
+  scale_grid_kernel<<<static_cast<unsigned>((K * n_alpha + 255) / 256), 256, 0, ps>>>(ga);
+  AWQ_TRY(launched(AWQ_K_SCALE_GRID, ps));
   // 3. max |W| for the residual's power-of-two scale
-  if (cudaMemsetAsync(absmax, 0, sizeof(unsigned int), st) != cudaSuccess) {
+  if (cudaMemsetAsync(absmax, 0, sizeof(unsigned int), ps) != cudaSuccess) {
     cudaGetLastError();
     return AWQ_ERR_CUDA;
   }
   const long long n8 = N * K / 8;
   const unsigned agrid = static_cast<unsigned>(std::min<long long>(4LL * d->sms, (n8 + 255) / 256));
-  prof_start(AWQ_K_ABSMAX, st);
-  absmax_kernel<<<agrid, 256, 0, st>>>(W, n8, absmax);
-  AWQ_TRY(launched(AWQ_K_ABSMAX, st));
+  prof_start(AWQ_K_ABSMAX, ps);
+  absmax_kernel<<<agrid, 256, 0, ps>>>(W, n8, absmax);
+  AWQ_TRY(launched(AWQ_K_ABSMAX, ps));
   // 4. Gram schedule: X^T and its column sums of squares, max_k H[k][k], then the scaled lower
   //    triangle of H = X^T X (once per layer)
   auto smem_attr = [](const void* f, int bytes) -> awq_status_t {
@@ -973,6 +983,11 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     gram::colsq_max_kernel<<<static_cast<unsigned>((K + 31) / 32), 256, 0, st>>>(
         colsq, nblk, static_cast<int>(K), hmax);
     AWQ_TRY(launched(AWQ_K_GRAM_PREP, st));
+    if (cudaEventRecord(d->score_done[0], ps) != cudaSuccess ||
+        cudaStreamWaitEvent(st, d->score_done[0], 0) != cudaSuccess) {  // join
+      cudaGetLastError();
+      return AWQ_ERR_CUDA;
+    }
     if (score_mode != AWQ_SCORE_GRAM_LAUNCHES) {
       AWQ_TRY(launch_search_persistent(cfg.group_size, d, L, ws, Xt, Bm, hmax, Dbuf, W, absmax,
                                        s_grid, inv_grid, partial, N, K, n_alpha, cfg.symmetric,
