@@ -483,3 +483,36 @@ def test_bounded_waits_give_up_and_recover():
     for a, b in zip(want, got):
         for u, v in zip(a, b):
             assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("mode", ["gram", "gram_launches", "direct"])
+def test_search_captured_in_a_cuda_graph(mode):
+    """After a first eager call, the whole search (its second stream included) captures into a
+    CUDA graph; replays give the eager call's bits."""
+    d = layer(51, 700, 1024, 2048, n_out=8)
+    W, X = dev(d["W"]), dev(d["X"])
+    N, K = W.shape
+    T = X.shape[0]
+    alphas = synth.alpha_grid(20)
+    with score_mode(mode):
+        want = awq.search_scale(W, X, alphas)
+        ws_bytes = awq.awq_search_workspace_bytes(N, K, T, 20)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        err = torch.empty(20, dtype=torch.float32, device="cuda")
+        best = torch.empty(1, dtype=torch.int32, device="cuda")
+        s = torch.empty(K, dtype=torch.float32, device="cuda")
+        inv = torch.empty(K, dtype=torch.float32, device="cuda")
+        stream = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                awq.awq_search_scale(W, N, K, X, T, None, alphas, 20, 128, False, ws, ws_bytes, err,
+                                     best, s, inv, stream)
+        for _ in range(2):
+            err.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            awq.awq_stream_status()
+            for u, v in zip(want, (err, best, s, inv)):
+                assert torch.equal(u, v)
