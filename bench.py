@@ -86,15 +86,26 @@ def layer_units(wl_name):
     return wl, spec
 
 
-def profiled_traffic(profile_md, source):
-    """DRAM bytes per launch from a committed ncu summary, or None when the kernel source has
-    changed since the counters were taken (its sha256 prefix no longer matches)."""
+def source_digest(sources):
+    """sha256 prefix of the kernel's source files (under the package's csrc/), concatenated in
+    the given order; None if one is missing."""
     import hashlib
+    h = hashlib.sha256()
+    for name in sources:
+        src = os.path.join(ROOT, "post_weight_quantization_stats_b300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_md, sources):
+    """DRAM bytes per launch from a committed ncu summary, or None when any source the kernel
+    is built from has changed since the counters were taken (the digest no longer matches)."""
     path = os.path.join(ROOT, "profiles", profile_md)
-    src = os.path.join(ROOT, "post_weight_quantization_stats_b300", "csrc", source)
-    if not (os.path.exists(path) and os.path.exists(src)):
+    sha = source_digest(sources)
+    if sha is None or not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     text = open(path).read()
     want, traffic = None, None
     for line in text.splitlines():
@@ -703,16 +714,16 @@ ROOFLINE_KERNELS = {
     "gram_search": ("search_kernel: one persistent cooperative launch, tcgen05 kind::f16 X^T X "
                     "triangle then D B^T over the triangle per alpha, next residual built in "
                     "extra warps", "tensor", "gram_search_llama7b_attn_4096.md",
-                    "gram_persistent.cuh"),
+                    ("gram_persistent.cuh", "gram_score.cuh", "quant.cuh")),
     "score_gram": ("tri_kernel<SCORE>: tcgen05 kind::f16 D B^T over the triangle, fp32 "
                    "accumulate, d . (D B^T) epilogue", "tensor",
-                   "score_gram_llama7b_attn_4096.md", "gram_score.cuh"),
+                   "score_gram_llama7b_attn_4096.md", ("gram_score.cuh", "quant.cuh")),
     "gram": ("tri_kernel<GRAM>: tcgen05 kind::f16 lower triangle of X^T X", "tensor",
-             "gram_llama7b_attn_4096.md", "gram_score.cuh"),
+             "gram_llama7b_attn_4096.md", ("gram_score.cuh", "quant.cuh")),
     "score": ("score_kernel: tcgen05 kind::f16 X D^T, fp32 accumulate, sum of squares", "tensor",
-              "score_kernel_llama7b_attn_4096.md", "score_gemm.cuh"),
+              "score_kernel_llama7b_attn_4096.md", ("score_gemm.cuh",)),
     "residual": ("residual_kernel: W - Q(W diag s) diag(s)^-1 as fp16", "hbm",
-                 "residual_kernel_llama7b_attn_4096.md", "quant.cuh"),
+                 "residual_kernel_llama7b_attn_4096.md", ("quant.cuh",)),
 }
 
 

@@ -164,6 +164,26 @@ awq_status_t awq_quantize_pack(const void* W_f16, int64_t N, int64_t K, const fl
                                uint8_t* zeros, awq_stream_t stream);
 
 /*
+ * The quantisation residual of one scale vector: the operand the search scores, one candidate
+ * of "AWQ Math", "Searching the scale" (the output error of that candidate is the mean of
+ * (X D^T)^2 / 2^(2p) over tokens and outputs).
+ *   D = 2^p (W - w_hat),  w_hat = (q - z) step16 / s  element by element,
+ * with q, z and step the codes, zero points and fp32 steps awq_quantize_pack produces for s,
+ * step16 = fp16(step), the products and the difference IEEE fp32 operations in that order and
+ * the result rounded once to fp16; p = 14 - e where max|W| < 2^e <= 2 max|W| (p = 0 for an
+ * all-zero W), so that every |D| < 2^14 (|W - w_hat| <= |W| for every weight).
+ *   W_f16       [N, K] fp16 row-major
+ *   s, inv_s    [K] fp32, both required: the scale and 1 / s (IEEE division), 16-byte aligned
+ *   absmax_bits [1] device uint32 out: the fp32 bit pattern of max|W|, from which the caller
+ *               reads p; it is also the call's scratch
+ *   D_f16       [N, K] fp16 out
+ * Two kernels on `stream` (max|W|, then the residual); the search builds the same residual.
+ */
+awq_status_t awq_quant_residual(const void* W_f16, int64_t N, int64_t K, const float* s,
+                                const float* inv_s, awq_qcfg_t cfg, uint32_t* absmax_bits,
+                                void* D_f16, awq_stream_t stream);
+
+/*
  * W4A16 dequant-fused matmul: Y [M, N] fp16 = X [M, K] fp16 @ (dequant(Q) diag(inv_s))^T,
  * fp32 accumulation. inv_s [K] fp32 or NULL (1/s already folded into the previous layer).
  * M <= 8 runs a CUDA-core GEMV; larger M runs the tcgen05 tensor-core kernel. With inv_s,

@@ -239,6 +239,26 @@ def error_of_codes(X: np.ndarray, W: np.ndarray, qweight, scales, zeros, s,
     return output_mse(X, W, w_hat)
 
 
+def residual(W: np.ndarray, s, group_size: int = 128, symmetric: bool = False) -> np.ndarray:
+    """D = W - Q(W diag(s)) diag(s)^-1 in fp64: the weight error of one candidate, whose product
+    with the calibration inputs is that candidate's output error, since
+    W x - Q(W diag(s)) diag(s)^-1 x = D x ("AWQ Math", "Searching the scale")."""
+    qd = quantize_pack(W, s, group_size, symmetric)
+    w_hat = dequantize(qd["qweight"], qd["scales"], qd["zeros"], group_size, s=s)
+    return np.asarray(W, dtype=np.float64) - w_hat
+
+
+def residual_exponent(W: np.ndarray) -> int:
+    """p with max|W| < 2^(14 - p) <= 2 max|W| (0 for an all-zero W): the power-of-two factor the
+    GPU applies to D before rounding it to fp16, which keeps every |2^p D| below 2^14 because
+    |D| <= |W| element by element."""
+    mx = float(np.max(np.abs(np.asarray(W, dtype=np.float64)))) if np.size(W) else 0.0
+    if mx == 0.0:
+        return 0
+    _, e = np.frexp(mx)            # mx = f 2^e, f in [0.5, 1)
+    return 14 - int(e)
+
+
 # ----------------------------------------------------------------------------------------
 # W4A16 dequant-fused matmul ("AWQ > Benefits and Practical Considerations")
 # ----------------------------------------------------------------------------------------

@@ -52,6 +52,8 @@ _SIGNATURES = {
                                                _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "awq_quantize_pack": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, QCfg, _c_void_p,
                                          _c_void_p, _c_void_p, _c_void_p]),
+    "awq_quant_residual": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, QCfg,
+                                          _c_void_p, _c_void_p, _c_void_p]),
     "awq_w4a16_gemm": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
                                       _c_void_p, _c_void_p, QCfg, _c_void_p, _c_void_p]),
     "awq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -163,6 +165,12 @@ def awq_quantize_pack(W, N, K, s, group_size, symmetric, qweight, scales, zeros,
         _ptr(zeros), _stream(stream)))
 
 
+def awq_quant_residual(W, N, K, s, inv_s, group_size, symmetric, absmax_bits, D, stream=None):
+    _check("awq_quant_residual", lib().awq_quant_residual(
+        _ptr(W), N, K, _ptr(s), _ptr(inv_s), _cfg(group_size, symmetric), _ptr(absmax_bits),
+        _ptr(D), _stream(stream)))
+
+
 def awq_w4a16_gemm(X, M, N, K, qweight, scales, zeros, inv_s, group_size, symmetric, Y,
                    stream=None):
     _check("awq_w4a16_gemm", lib().awq_w4a16_gemm(
@@ -240,6 +248,17 @@ def quantize_pack(W, s=None, group_size=128, symmetric=False, stream=None):
     z = torch.empty((K // group_size, N), dtype=torch.uint8, device=W.device)
     awq_quantize_pack(W, N, K, s, group_size, symmetric, q, sc, z, stream)
     return q, sc, z
+
+
+def quant_residual(W, s, inv_s, group_size=128, symmetric=False, stream=None):
+    """(D [N, K] fp16, absmax_bits [1] int32): D = 2^p (W - Q(W diag(s)) diag(s)^-1), p from
+    max|W| whose fp32 bits absmax_bits holds (see awq_quant_residual)."""
+    import torch
+    N, K = W.shape
+    D = torch.empty((N, K), dtype=torch.float16, device=W.device)
+    bits = torch.empty(1, dtype=torch.int32, device=W.device)
+    awq_quant_residual(W, N, K, s, inv_s, group_size, symmetric, bits, D, stream)
+    return D, bits
 
 
 def search_scale(W, X, alphas, group_size=128, symmetric=False, mean_abs=None, workspace=None,

@@ -809,6 +809,42 @@ awq_status_t awq_quantize_pack(const void* W_f16, int64_t N, int64_t K, const fl
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+awq_status_t awq_quant_residual(const void* W_f16, int64_t N, int64_t K, const float* s,
+                                const float* inv_s, awq_qcfg_t cfg, uint32_t* absmax_bits,
+                                void* D_f16, awq_stream_t stream) {
+  AWQ_TRY(check_cfg(cfg));
+  if (!W_f16 || !s || !inv_s || !absmax_bits || !D_f16) return AWQ_ERR_INVALID_ARG;
+  AWQ_TRY(check_nk(N, K, cfg));
+  if (!aligned16(W_f16) || !aligned16(s) || !aligned16(inv_s) || !aligned16(D_f16) ||
+      reinterpret_cast<uintptr_t>(absmax_bits) % 4 != 0)
+    return AWQ_ERR_MISALIGNED;
+  DeviceInfo* d = nullptr;
+  AWQ_TRY(device_info(&d));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const __half* W = static_cast<const __half*>(W_f16);
+  if (cudaMemsetAsync(absmax_bits, 0, sizeof(uint32_t), st) != cudaSuccess) {
+    cudaGetLastError();
+    return AWQ_ERR_CUDA;
+  }
+  const long long n8 = N * K / 8;
+  const unsigned agrid = static_cast<unsigned>(std::min<long long>(4LL * d->sms, (n8 + 255) / 256));
+  prof_start(AWQ_K_ABSMAX, st);
+  absmax_kernel<<<agrid, 256, 0, st>>>(W, n8, absmax_bits);
+  AWQ_TRY(launched(AWQ_K_ABSMAX, st));
+  const ResidualArgs ra{W, s, inv_s, absmax_bits, static_cast<__half*>(D_f16),
+                        static_cast<int>(N), static_cast<int>(K), cfg.symmetric};
+  const dim3 rgrid(static_cast<unsigned>((N + 8 * QROWS - 1) / (8 * QROWS)),
+                   static_cast<unsigned>((K / 8 + 31) / 32));
+  prof_start(AWQ_K_RESIDUAL, st);
+  if (cfg.group_size == 128)
+    residual_kernel<128><<<rgrid, 256, 0, st>>>(ra);
+  else if (cfg.group_size == 64)
+    residual_kernel<64><<<rgrid, 256, 0, st>>>(ra);
+  else
+    residual_kernel<32><<<rgrid, 256, 0, st>>>(ra);
+  return launched(AWQ_K_RESIDUAL, st);
+}
+
 }  // extern "C"
 
 namespace awq {

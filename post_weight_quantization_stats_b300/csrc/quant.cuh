@@ -45,12 +45,32 @@ __device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool s
   return group_params_of(lo, hi, symmetric);
 }
 
+// Round to the nearest integer, ties to even, for |x| < 2^22: x + 1.5 * 2^23 lies in a binade
+// whose unit in the last place is 1, so that IEEE addition rounds x itself (1.5 * 2^23 is even,
+// so ties land on even integers) and the subtraction is exact. Two full-rate adds.
+__device__ __forceinline__ float rint_small(float x) {
+  return __fsub_rn(__fadd_rn(x, 0x1.8p23f), 0x1.8p23f);
+}
+
+// fl32(d / 15) for d >= 0 without a division: q0 = fl32(d * r15) with r15 = fl32(1/15), the
+// remainder e = d - 15 q0 (exact in one FMA), and one correction q0 + e r15 rounded once
+// (Markstein's correction step, "IA-64 and Elementary Functions", 2000). The result is the
+// correctly rounded quotient for every d whose quotient is a normal float: the rounding
+// pattern of d / 15 depends only on d's significand, and all 2^23 significands were checked
+// against exact rational arithmetic. Smaller d take the IEEE division.
+__device__ __forceinline__ float div15(float d) {
+  constexpr float r15 = 0x1.111112p-4f;
+  if (d < 0x1p-100f) return __fdiv_rn(d, 15.0f);
+  const float q0 = __fmul_rn(d, r15);
+  return __fmaf_rn(__fmaf_rn(-q0, 15.0f, d), r15, q0);
+}
+
 // Step, zero point and reciprocal of a group from the min and max of its w'.
 __device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric) {
   GroupParams g;
   if (symmetric) {
     const float amax = fmaxf(hi, -lo);  // max |w'| of the group
-    float st = __fdiv_rn(amax, 8.0f);
+    float st = __fmul_rn(amax, 0.125f);  // = fl32(amax / 8): the same exact value, rounded once
     if (st == 0.0f) st = 1.0f;
     g.step = st;
     g.zero = 8.0f;
@@ -58,22 +78,17 @@ __device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool 
   } else {
     hi = fmaxf(hi, 0.0f);
     lo = fminf(lo, 0.0f);
-    float st = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+    float st = div15(__fsub_rn(hi, lo));
     if (st == 0.0f) st = 1.0f;
-    float z = rintf(__fdiv_rn(-lo, st));
-    z = fminf(fmaxf(z, 0.0f), 15.0f);
     g.step = st;
-    g.zero = z;
     g.rcp = __frcp_rn(st);
+    // rint(fl32(-lo / st)) as in rint_quotient: 0 <= -lo <= hi - lo, so the quotient is below 16
+    const float t = __fmul_rn(-lo, g.rcp);
+    float z = rint_small(t);
+    if (fabsf(__fsub_rn(t, z)) >= 0.5f - 0x1p-17f) z = rintf(__fdiv_rn(-lo, st));
+    g.zero = fminf(fmaxf(z, 0.0f), 15.0f);
   }
   return g;
-}
-
-// Round to the nearest integer, ties to even, for |x| < 2^22: x + 1.5 * 2^23 lies in a binade
-// whose unit in the last place is 1, so that IEEE addition rounds x itself (1.5 * 2^23 is even,
-// so ties land on even integers) and the subtraction is exact. Two full-rate adds.
-__device__ __forceinline__ float rint_small(float x) {
-  return __fsub_rn(__fadd_rn(x, 0x1.8p23f), 0x1.8p23f);
 }
 
 // rint(fl32(wp / step)) without a division in the common case. |wp / step| <= 15 for every
@@ -264,11 +279,11 @@ struct ResidualArgs {
 // keeps every residual inside the fp16 range.
 // One 8-warp block of the residual: warp `warp` (0..7) covers rows (rb * 8 + warp) * QROWS ..
 // + QROWS - 1, lane `lane` the packed word 32 chunk + lane of each. Split into the loads
-// (residual_load: the lane's QROWS weight words and 8 channels of s and 1/s) and the rest
-// (residual_store), so a caller can overlap the next block's loads with this block's work.
+// (residual_load: the lane's QROWS weight words, from HBM) and the rest (residual_store, which
+// reads the lane's 8 channels of s and 1/s, shared by every row and so cached), so a caller
+// can overlap the next block's weight loads with this block's work.
 struct ResidualRegs {
   uint4 raw[QROWS];
-  float sv[8], iv[8];
   int rbase, k0;
   bool wok;
 };
@@ -279,8 +294,6 @@ __device__ __forceinline__ void residual_load(const ResidualArgs& a, int rb, int
   r.wok = w < (a.K >> 3);
   r.k0 = (r.wok ? w : 0) * 8;
   r.rbase = (rb * 8 + warp) * QROWS;
-  load8f(a.s + r.k0, r.wok, 1.0f, r.sv);
-  load8f(a.inv_s + r.k0, r.wok, 1.0f, r.iv);
 #pragma unroll
   for (int q = 0; q < QROWS; ++q) {
     const int row = r.rbase + q;
@@ -290,38 +303,123 @@ __device__ __forceinline__ void residual_load(const ResidualArgs& a, int rb, int
   }
 }
 
+// The arithmetic runs in phases over RB rows at a time, so the rows' independent chains
+// interleave: w' and the lane's min/max; the team shuffles; the group parameters; the rounded
+// quotients, with one check per lane for a quotient near a rounding boundary (a single rare
+// branch instead of one per weight, redone with IEEE division for the lane's RB rows, which
+// gives the same integers everywhere else); then the codes, w_hat and the residual. RB is
+// bounded by the registers the calling kernel can spare.
+constexpr int RES_RB = 1;
+
+template <int TEAM, int RB>
+__device__ __forceinline__ void residual_rows(const ResidualArgs& a, const ResidualRegs& r, int q0,
+                                              const float (&sv)[8], const float (&iv)[8],
+                                              float p2) {
+  const bool sym = a.symmetric != 0;
+  float v[RB][8];  // w', then the rounded quotient rint(w' / step)
+  float lo[RB], hi[RB];
+#pragma unroll
+  for (int q = 0; q < RB; ++q) {
+    float wv[8];
+    unpack8(r.raw[q0 + q], wv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[q][i] = __fmul_rn(wv[i], sv[i]);
+    lo[q] = v[q][0];
+    hi[q] = v[q][0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      lo[q] = fminf(lo[q], v[q][i]);
+      hi[q] = fmaxf(hi[q], v[q][i]);
+    }
+  }
+#pragma unroll
+  for (int o = TEAM / 2; o >= 1; o >>= 1) {
+#pragma unroll
+    for (int q = 0; q < RB; ++q) {
+      lo[q] = fminf(lo[q], __shfl_xor_sync(0xffffffffu, lo[q], o));
+      hi[q] = fmaxf(hi[q], __shfl_xor_sync(0xffffffffu, hi[q], o));
+    }
+  }
+  GroupParams g[RB];
+#pragma unroll
+  for (int q = 0; q < RB; ++q) g[q] = group_params_of(lo[q], hi[q], sym);
+  // The integers are carried shifted by kM = 1.5 * 2^23, where the unit in the last place is 1:
+  // u = fl32(w' rcp + kM) = kM + rint(w' rcp) in one FMA, and kM - u = -rint(w' rcp) exactly,
+  // so fma(w', rcp, kM - u) is w' rcp - rint(w' rcp) rounded once. Where that lies within
+  // 2^-17 of +-1/2 the exact product w' rcp (within 2^-19 of the quotient, like t in
+  // rint_quotient) may round differently from fl32(w' / step); elsewhere both give rint_quotient's
+  // integer.
+  constexpr float kM = 0x1.8p23f;
+  bool edge = false;
+#pragma unroll
+  for (int q = 0; q < RB; ++q) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float u = __fmaf_rn(v[q][i], g[q].rcp, kM);
+      edge |= fabsf(__fmaf_rn(v[q][i], g[q].rcp, __fsub_rn(kM, u))) >= 0.5f - 0x1p-17f;
+      v[q][i] = u;
+    }
+  }
+  if (edge) {  // see rint_quotient
+#pragma unroll
+    for (int q = 0; q < RB; ++q) {
+      float wv[8];
+      unpack8(r.raw[q0 + q], wv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[q][i] = __fadd_rn(rintf(__fdiv_rn(__fmul_rn(wv[i], sv[i]), g[q].step)), kM);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < RB; ++q) {
+    const int row = r.rbase + q0 + q;
+    // kM + (code - zero), clamped as code_f clamps the code (exact small integers plus kM)
+    const float ulo = __fadd_rn(kM, sym ? -8.0f : -g[q].zero);
+    const float uhi = __fadd_rn(kM, sym ? 7.0f : __fsub_rn(15.0f, g[q].zero));
+    // With sp = step16 p2 (p2 a power of two, so exact): fma(u, sp, -kM sp) = (code - zero) sp
+    // exactly (an integer below 16 times an 11-bit significand), times 1/s rounded once is
+    // fl32((code - zero) step16 / s) p2 = w_hat p2, and fma(w, p2, -w_hat p2) =
+    // fl32(w - w_hat) p2: the same bits as scaling after each rounding.
+    const float sp = __fmul_rn(__half2float(__float2half_rn(g[q].step)), p2);
+    const float msp = -__fmul_rn(kM, sp);
+    float wv[8];
+    unpack8(r.raw[q0 + q], wv);
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      float d2[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float uc = fminf(fmaxf(v[q][i + j], ulo), uhi);
+        const float w_hat_p2 = __fmul_rn(__fmaf_rn(uc, sp, msp), iv[i + j]);
+        d2[j] = __fmaf_rn(wv[i + j], p2, -w_hat_p2);
+      }
+      const __half2 h = __floats2half2_rn(d2[0], d2[1]);
+      memcpy(&out[i / 2], &h, sizeof(uint32_t));
+    }
+    if (r.wok && row < a.N)
+      *reinterpret_cast<uint4*>(a.D + static_cast<long long>(row) * a.K + r.k0) =
+          make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// One block's residual given the lane's 8 channels of s and 1/s.
+template <int G>
+__device__ __forceinline__ void residual_compute(const ResidualArgs& a, const ResidualRegs& r,
+                                                 const float (&sv)[8], const float (&iv)[8],
+                                                 float p2) {
+  static_assert(QROWS % RES_RB == 0, "row batches must tile the rows");
+#pragma unroll
+  for (int q0 = 0; q0 < QROWS; q0 += RES_RB) residual_rows<G / 8, RES_RB>(a, r, q0, sv, iv, p2);
+}
+
 template <int G>
 __device__ __forceinline__ void residual_store(const ResidualArgs& a, const ResidualRegs& r,
                                                float p2) {
-  constexpr int TEAM = G / 8;
-  const bool sym = a.symmetric != 0;
-#pragma unroll
-  for (int q = 0; q < QROWS; ++q) {
-    const int row = r.rbase + q;
-    float wv[8], wp[8];
-    unpack8(r.raw[q], wv);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) wp[i] = __fmul_rn(wv[i], r.sv[i]);
-    const GroupParams g = group_params<TEAM>(wp, sym);   // every lane takes part in the shuffles
-    if (r.wok && row < a.N) {
-      const float step16 = __half2float(__float2half_rn(g.step));
-      uint32_t out[4];
-#pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        float d2[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float qz = __fsub_rn(code_f(wp[i + j], g, sym), g.zero);  // exact
-          const float w_hat = __fmul_rn(__fmul_rn(qz, step16), r.iv[i + j]);
-          d2[j] = __fmul_rn(__fsub_rn(wv[i + j], w_hat), p2);
-        }
-        const __half2 h = __floats2half2_rn(d2[0], d2[1]);
-        memcpy(&out[i / 2], &h, sizeof(uint32_t));
-      }
-      *reinterpret_cast<uint4*>(a.D + static_cast<long long>(row) * a.K + r.k0) =
-          make_uint4(out[0], out[1], out[2], out[3]);
-    }
-  }
+  float sv[8], iv[8];
+  load8f(a.s + r.k0, r.wok, 1.0f, sv);
+  load8f(a.inv_s + r.k0, r.wok, 1.0f, iv);
+  residual_compute<G>(a, r, sv, iv, p2);
 }
 
 // Row blocks of 8 * QROWS rows on grid x, 256-channel column chunks on grid y.

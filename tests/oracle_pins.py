@@ -339,6 +339,38 @@ def pin_search(o):
 
 # ------------------------------------------------------------------ W4A16 matmul
 
+def pin_residual(o):
+    """D = W - Q(W diag(s)) diag(s)^-1, the weight error one candidate is scored by ("Searching
+    the scale"): on a group with lo = -7/16 and hi = 1/2 (step 1/16, zero point 7) the half-way
+    weights (0.5, 1.5, 2.5, -0.5, -1.5) / 16 round to even and leave +-1/32 with the matching
+    sign, while the on-grid weights leave 0; symmetric, 1/2 clamps to 7 steps and leaves 1/16.
+    Scaling by powers of two commutes with it; |D| <= |W| everywhere (so 2^p D fits fp16)."""
+    G = 128
+    W = np.zeros((1, G), np.float16)
+    W[0, :7] = np.array([-7.0, 8.0, 0.5, 1.5, 2.5, -0.5, -1.5]) / 16
+    W[0, 7:23] = (np.arange(16) - 7) / 16.0
+    one = np.ones(G, np.float32)
+    D = o.residual(W, one, G, False)
+    assert np.array_equal(D[0, :7] * 32, [0, 0, 1, -1, 1, -1, 1])
+    assert np.all(D[0, 7:] == 0)
+    Ds = o.residual(W, one, G, True)
+    assert np.array_equal(Ds[0, :7] * 32, [0, 2, 1, -1, 1, -1, 1])
+    two = np.where(np.arange(G) % 3 == 0, 4.0, 0.5).astype(np.float32)
+    # per-channel powers of two move each weight's quotient, not D's definition: w_hat * s is
+    # the same level grid for W' = W s, so D s is the residual of W' with s = 1
+    Wp = (W.astype(np.float64) * two).astype(np.float16)
+    assert np.array_equal(o.residual(W, two, G, False) * two, o.residual(Wp, one, G, False))
+    Wb, sb = _bound_cases()
+    for sym in (False, True):
+        for gs in (64, 128):
+            Db = o.residual(Wb, sb, gs, sym)
+            assert np.all(np.abs(Db) <= np.abs(Wb.astype(np.float64)) * (1 + 2.0 ** -20))
+    assert o.residual_exponent(W) == 14          # max|W| = 1/2 < 2^0
+    assert o.residual_exponent(np.array([[1.0, -0.25]], np.float16)) == 13
+    assert o.residual_exponent(np.array([[-65504.0]], np.float16)) == -2
+    assert o.residual_exponent(np.zeros((2, 8), np.float16)) == 0
+
+
 def pin_gemm_closed_form(o):
     """Dequant-fused matmul: codes z+1 with step 1 give w_hat = 1, so Y is the row sums of X
     (times inv_s when given) ("Benefits ...": unpack, group scale, zero point, inverse scale)."""

@@ -112,6 +112,16 @@ def test_host_validation_rejects_without_cuda(L):
         S["AWQ_ERR_INVALID_ARG"]
     assert _code(L, "awq_w4a16_gemm", A, 4, 16, 256, A, A, A, None, cfg, A + 8, None) == \
         S["AWQ_ERR_MISALIGNED"]
+    assert _code(L, "awq_quant_residual", A, 16, 256, None, A, cfg, A, A, None) == \
+        S["AWQ_ERR_INVALID_ARG"]                          # s is required
+    assert _code(L, "awq_quant_residual", A, 16, 256, A, A, cfg, None, A, None) == \
+        S["AWQ_ERR_INVALID_ARG"]                          # so is the max|W| word
+    assert _code(L, "awq_quant_residual", A, 16, 100, A, A, cfg, A, A, None) == \
+        S["AWQ_ERR_UNSUPPORTED_SHAPE"]
+    assert _code(L, "awq_quant_residual", A, 16, 256, A, A + 4, cfg, A, A, None) == \
+        S["AWQ_ERR_MISALIGNED"]
+    assert _code(L, "awq_quant_residual", A, 16, 256, A, A, cfg, A + 2, A, None) == \
+        S["AWQ_ERR_MISALIGNED"]
     alphas = (ctypes.c_float * 2)(0.0, 0.5)
     ap = ctypes.cast(alphas, ctypes.c_void_p)
     ws = awq.awq_search_workspace_bytes(16, 256, 8, 2)
@@ -133,6 +143,8 @@ def test_valid_call_without_a_gpu_reports_no_device(L):
     cfg = awq.QCfg(128, 0)
     A = 1 << 20
     assert _code(L, "awq_quantize_pack", A, 16, 256, None, cfg, A, A, A, None) == \
+        awq.STATUS_CODE["AWQ_ERR_NO_DEVICE"]
+    assert _code(L, "awq_quant_residual", A, 16, 256, A, A, cfg, A, A, None) == \
         awq.STATUS_CODE["AWQ_ERR_NO_DEVICE"]
 
 

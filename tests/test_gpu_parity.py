@@ -203,6 +203,80 @@ def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False, gram=False):
     return e, b, r
 
 
+# ----------------------------------------------------------------------------- residual
+
+def _ulp16(x):
+    """fp16's spacing at |x| (2^-24 below the normal range)."""
+    m = np.maximum(np.abs(x), 2.0 ** -14)
+    return 2.0 ** (np.floor(np.log2(m)) - 10)
+
+
+def _check_residual(W, s, G, sym):
+    """The GPU's 2^p (W - w_hat) against the oracle's fp64 residual: within one fp16 spacing
+    plus the fp32 roundings of w_hat and of the difference (2^-21 |w_hat| scaled). A code that
+    differs from the oracle's moves D by a whole step, and a tie broken the other way flips the
+    sign of a half step: both far outside that bound. max|W| comes back bit-exact."""
+    inv = (np.float32(1) / s).astype(np.float32)
+    D, bits = awq.quant_residual(dev(W), dev(s), dev(inv), G, sym)
+    awq.awq_stream_status()
+    mx = np.float32(np.max(np.abs(W.astype(np.float32))))
+    assert host(bits).view(np.uint32)[0] == mx.view(np.uint32)
+    p = ref.residual_exponent(W)
+    qd = ref.quantize_pack(W, s, G, sym)
+    w_hat = ref.dequantize(qd["qweight"], qd["scales"], qd["zeros"], G, s=s)
+    exact = (W.astype(np.float64) - w_hat) * 2.0 ** p
+    got = host(D).astype(np.float64)
+    tol = _ulp16(np.maximum(np.abs(got), np.abs(exact))) + np.abs(w_hat) * 2.0 ** (p - 21)
+    bad = np.abs(got - exact) > tol
+    assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:5], got[bad][:5], exact[bad][:5])
+    assert np.all(np.abs(got) < 2.0 ** 14)
+
+
+@pytest.mark.parametrize("N,K,G,sym", [(300, 832, 32, False), (513, 2048, 128, False),
+                                       (256, 512, 64, True), (1, 128, 128, False),
+                                       (77, 384, 128, True), (40, 1024, 64, False)])
+def test_quant_residual_matches_oracle(N, K, G, sym):
+    rng = np.random.Generator(np.random.PCG64(N + K + G))
+    W = synth.draw_weight(rng, N, K, 0.02)
+    s = np.exp(rng.uniform(-3.0, 3.0, K)).astype(np.float32)
+    _check_residual(W, s, G, sym)
+
+
+def test_quant_residual_special_groups():
+    """Exact half-way quotients (ties to even), on-grid weights, all-zero, constant, one-signed
+    and large groups, with s = 1 and with per-channel powers of two (quotients unchanged)."""
+    K = 256
+    W = np.zeros((8, K), np.float16)
+    W[0, :7] = np.array([-7.0, 8.0, 0.5, 1.5, 2.5, -0.5, -1.5]) / 16
+    W[0, 7:128] = ((np.arange(121) % 31) - 15) / 32.0
+    W[0, 128:] = (np.arange(128) % 16 - 7) / 16.0
+    W[1] = 0.5
+    W[2, :128] = -np.linspace(0.01, 1, 128)
+    W[2, 128:] = np.linspace(0.01, 1, 128)
+    W[3] = (np.arange(K) % 31 - 15) * 2.0 ** -5
+    W[4] = (np.arange(K) % 16) * 2.0 ** -6
+    W[5, ::2] = 65504.0 / 4
+    W[6, ::3] = -3.0
+    W = W.astype(np.float16)
+    pow2 = np.where(np.arange(K) % 5 == 0, 8.0, 0.25).astype(np.float32)
+    for s in (np.ones(K, np.float32), pow2):
+        for sym in (False, True):
+            for G in (32, 64, 128):
+                _check_residual(W, s, G, sym)
+
+
+def test_quant_residual_near_ties_full_size():
+    """8M weights with scales from a real alpha grid: about 1.5e-5 of the quotients fall near
+    a rounding boundary, where the kernel takes the IEEE division instead of the reciprocal;
+    every element still matches the oracle."""
+    d = synth.make_layer("llama7b-attn-4096")
+    W = d["W"][:2048]
+    m = ref.calib_stats(d["X"][:512])
+    for a in (0.35, 0.8):
+        s = ref.fl32(ref.scale_grid(m, [a]))[0].astype(np.float32)
+        _check_residual(W, s, 128, False)
+
+
 def test_search_tiny_layer():
     d = synth.make_layer("tiny-512")
     e, b, r = _check_search(d["W"], d["X"], synth.alpha_grid(20))

@@ -33,6 +33,9 @@ MUTATIONS = {
     "wrong group index": ("g_of_k = np.arange(K) // group_size",
                           "g_of_k = np.arange(K) % (K // group_size)"),
     "nibble order reversed in pack": ("<< np.uint64(4 * i)", "<< np.uint64(4 * (7 - i))"),
+    "residual adds the dequantised weight": ("np.asarray(W, dtype=np.float64) - w_hat",
+                                             "np.asarray(W, dtype=np.float64) + w_hat"),
+    "residual exponent off by one": ("return 14 - int(e)", "return 15 - int(e)"),
     "statistic drops the absolute value": ("total += np.abs(X64[t])", "total += X64[t]"),
     "statistic divides by T - 1": ("return total / T", "return total / (T - 1)"),
     "statistic uses the max": ("total += np.abs(X64[t])",
