@@ -3,7 +3,7 @@
 // Same arithmetic as tri_kernel (gram_score.cuh), phase by phase: phase 0 forms the scaled
 // triangle B of H = X^T X, phase 1 + a scores candidate a through it ("AWQ Math", "Searching the
 // scale"). Every CTA walks the same phase sequence with the same roles (warp 0 TMA producer,
-// warp 1 MMA issuer, warps 2-5 epilogue, warps 6-13 residual builders) and the same serpentine
+// warp 1 MMA issuer, warps 2-5 epilogue, warps 6-15 residual builders) and the same serpentine
 // tile deal, so each CTA's fp64 partials are summed in a fixed order, as with one launch per
 // phase (a phase's tiles go to its first min(tiles, CTAs) CTAs, the grid of the launch that
 // phase would get, so both schedules give the same bits). What one launch per phase got from
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= 6) {
     // residual a is built during phase a (the triangle's phase for a = 0), into buffer a % 2,
     // once every CTA is done reading that buffer for candidate a - 2
-    constexpr int TW = 8;  // warps per residual block
+    constexpr int TW = RES_WARPS;  // warps per residual block
     const int rw = warp - 6;
     const int chunks = (p.K / 8 + 31) / 32;
     const int items = (p.N + TW * QROWS - 1) / (TW * QROWS) * chunks;
@@ -245,10 +245,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         ra.D = p.D[a & 1];
         int item = cta;
         ResidualRegs cur, nxt;
-        if (item < items) residual_load(ra, item / chunks, item % chunks, rw, lane, cur);
+        if (item < items) residual_load(ra, item / chunks, item % chunks, rw, lane, cur, TW);
         for (; item < items; item += P) {
           const int next = item + P;
-          if (next < items) residual_load(ra, next / chunks, next % chunks, rw, lane, nxt);
+          if (next < items) residual_load(ra, next / chunks, next % chunks, rw, lane, nxt, TW);
           residual_store<G>(ra, cur, p2);
           if (next < items) cur = nxt;
         }

@@ -23,9 +23,9 @@
 // the CTAs in a fixed serpentine order (CTA c takes list positions c, 2P-1-c, 2P+c, ...); each
 // CTA's partial sums its tiles in that order, so the result does not depend on timing.
 //
-// Warps 6-13 build the residual of the NEXT candidate meanwhile (the GRAM launch builds
+// Warps 6-15 build the residual of the NEXT candidate meanwhile (the GRAM launch builds
 // candidate 0's, the SCORE launch of candidate i builds candidate i + 1's) into the other of two
-// residual buffers: 8-warp residual blocks (quant.cuh) dealt round-robin over the CTAs. The kernel
+// residual buffers: 10-warp residual blocks (quant.cuh) dealt round-robin over the CTAs. The kernel
 // boundary orders that residual before its own scoring launch, so no launch waits on another.
 #pragma once
 
@@ -42,8 +42,7 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int RES_TEAMS = 1;                // 8-warp residual teams
-constexpr int RES_WARPS = 8 * RES_TEAMS;
+constexpr int RES_WARPS = 10;               // residual warps: one block is RES_WARPS * QROWS rows
 constexpr int THREADS = 192 + 32 * RES_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
@@ -215,19 +214,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 6) {
     if (p.res_on) {
-      // team tm of 8 warps takes blocks cta * RES_TEAMS + tm, + P * RES_TEAMS, ...; the next
-      // block's loads are issued before this block's arithmetic
-      const int tm = (warp - 6) >> 3, rw = (warp - 6) & 7;
+      // the residual warps take blocks cta, cta + P, ...; the next block's loads are issued
+      // before this block's arithmetic
+      const int rw = warp - 6;
       const int chunks = (p.res.K / 8 + 31) / 32;
-      const int items = (p.res.N + 8 * QROWS - 1) / (8 * QROWS) * chunks;
-      const int stride = P * RES_TEAMS;
+      const int items = (p.res.N + RES_WARPS * QROWS - 1) / (RES_WARPS * QROWS) * chunks;
+      const int stride = P;
       const float p2 = ldexpf(1.0f, residual_exponent(*p.res.absmax));
-      int item = cta * RES_TEAMS + tm;
+      int item = cta;
       ResidualRegs cur, nxt;
-      if (item < items) residual_load(p.res, item / chunks, item % chunks, rw, lane, cur);
+      if (item < items) residual_load(p.res, item / chunks, item % chunks, rw, lane, cur, RES_WARPS);
       for (; item < items; item += stride) {
         const int next = item + stride;
-        if (next < items) residual_load(p.res, next / chunks, next % chunks, rw, lane, nxt);
+        if (next < items)
+          residual_load(p.res, next / chunks, next % chunks, rw, lane, nxt, RES_WARPS);
         residual_store<G>(p.res, cur, p2);
         if (next < items) cur = nxt;
       }

@@ -277,8 +277,8 @@ struct ResidualArgs {
 // so either the error is at most step/(2 s) <= |w| or it equals |w|; a clamped code sits at
 // least 7.5 steps out, where the one-step error is below |w'| too. Hence 2^p max|W| < 2^14
 // keeps every residual inside the fp16 range.
-// One 8-warp block of the residual: warp `warp` (0..7) covers rows (rb * 8 + warp) * QROWS ..
-// + QROWS - 1, lane `lane` the packed word 32 chunk + lane of each. Split into the loads
+// One block of the residual, `warps` warps high (8 in residual_kernel): warp `warp` covers rows
+// (rb * warps + warp) * QROWS .. + QROWS - 1, lane `lane` the packed word 32 chunk + lane of each. Split into the loads
 // (residual_load: the lane's QROWS weight words, from HBM) and the rest (residual_store, which
 // reads the lane's 8 channels of s and 1/s, shared by every row and so cached), so a caller
 // can overlap the next block's weight loads with this block's work.
@@ -289,11 +289,11 @@ struct ResidualRegs {
 };
 
 __device__ __forceinline__ void residual_load(const ResidualArgs& a, int rb, int chunk, int warp,
-                                              int lane, ResidualRegs& r) {
+                                              int lane, ResidualRegs& r, int warps = 8) {
   const int w = chunk * 32 + lane;
   r.wok = w < (a.K >> 3);
   r.k0 = (r.wok ? w : 0) * 8;
-  r.rbase = (rb * 8 + warp) * QROWS;
+  r.rbase = (rb * warps + warp) * QROWS;
 #pragma unroll
   for (int q = 0; q < QROWS; ++q) {
     const int row = r.rbase + q;
