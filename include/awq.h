@@ -70,7 +70,13 @@ typedef enum {
 
 typedef struct {
   int32_t group_size; /* 32, 64 or 128 input channels per (step, zero point) */
-  int32_t symmetric;  /* 0: asymmetric with zero point; 1: step = max|w| / 8, zero point 8 */
+  int32_t symmetric;  /* 0: asymmetric with zero point; 1: step = max|w| / 2^(bits-1) */
+  int32_t bits;       /* code width N of "Weight-only quantization" (D = max|w| / 2^(N-1)):
+                         0 or 4 for 4-bit codes, 3 or 2 for the narrower variants. Codes of
+                         every width are stored in the 4-bit nibbles of the packed format, so
+                         the matmul reads them unchanged: asymmetric codes 0 .. 2^N - 1 with a
+                         zero point in that range; symmetric q in [-2^(N-1), 2^(N-1) - 1]
+                         stored as q + 8 (implicit zero point 8 for every width) */
 } awq_qcfg_t;
 
 /*

@@ -30,6 +30,10 @@ Readings where the pages are silent (each is listed in the design notes):
 * Asymmetric quantiser (the pages name a step and a zero point but print no formula): the
   group range is widened to include 0, D = (hi - lo) / (2^4 - 1), z = clamp(rint(-lo / D)),
   q = clamp(rint(w / D) + z, 0, 15); D = 1 for an all-zero group.
+* Bit width N (the pages' D = max|w| / 2^(N-1) is written for any N; 4 is the default, 3 and 2
+  are the narrower variants): asymmetric codes 0..2^N - 1, symmetric q in [-2^(N-1), 2^(N-1) - 1];
+  codes of every width are stored in 4-bit nibbles (no denser packing), so the matmul reads them
+  unchanged.
 * Symmetric quantiser: the printed D = max|w| / 8 with codes clamped to [-8, 7] (4 bits hold
   16 levels); stored as q + 8 with an implicit zero point of 8.
 * rint is round-half-to-even; the stored step is fp16 (round to nearest even); codes are
@@ -49,8 +53,8 @@ from __future__ import annotations
 import numpy as np
 
 EPS = 1e-6        # floor on the statistic before the power (dead channels)
-QMAX_ASYM = 15    # 2^4 - 1 levels above the lowest
-SYM_DIV = 8.0     # 2^(N-1) for N = 4
+BITS = (2, 3, 4)  # code widths N; codes of every width are stored in 4-bit nibbles
+SYM_ZERO = 8      # implicit zero point of the stored symmetric codes (q + 8), for every width
 
 
 def fl32(a) -> np.ndarray:
@@ -96,13 +100,18 @@ def scaled_weight(W: np.ndarray, s) -> np.ndarray:
     return fl32(W64 * s32[None, :])
 
 
-def quantize(W: np.ndarray, s=None, group_size: int = 128, symmetric: bool = False) -> dict:
-    """Quantise W diag(s) group-wise to 4-bit codes.
+def quantize(W: np.ndarray, s=None, group_size: int = 128, symmetric: bool = False,
+             bits: int = 4) -> dict:
+    """Quantise W diag(s) group-wise to ``bits``-wide codes (N in "Weight-only quantization").
 
-    Returns ``codes`` [N, K] (stored nibble values 0..15), ``step32`` [N, K/G] (fp32 step the
-    codes were decided with), ``step16`` [N, K/G] (stored fp16 step), ``zero`` [N, K/G]
-    (uint8; 8 in symmetric mode) and ``clamped`` [N, K] (True where a clamp changed the code).
+    Returns ``codes`` [N, K] (stored nibble values), ``step32`` [N, K/G] (fp32 step the codes
+    were decided with), ``step16`` [N, K/G] (stored fp16 step), ``zero`` [N, K/G] (uint8; 8 in
+    symmetric mode) and ``clamped`` [N, K] (True where a clamp changed the code).
     """
+    if bits not in BITS:
+        raise ValueError("bits must be 2, 3 or 4")
+    qmax = 2 ** bits - 1              # asymmetric levels 0 .. qmax
+    half = 2 ** (bits - 1)            # symmetric: step = max|w'| / 2^(N-1), q in [-half, half-1]
     wp = scaled_weight(W, s).astype(np.float64)          # exact fp32 values held in fp64
     N, K = wp.shape
     if K % group_size:
@@ -110,22 +119,22 @@ def quantize(W: np.ndarray, s=None, group_size: int = 128, symmetric: bool = Fal
     grp = wp.reshape(N, K // group_size, group_size)
     if symmetric:
         amax = np.max(np.abs(grp), axis=2)
-        step = fl32(amax / SYM_DIV).astype(np.float64)
+        step = fl32(amax / half).astype(np.float64)
         step[step == 0.0] = 1.0
         r = np.rint(fl32(grp / step[:, :, None]).astype(np.float64))
-        q = np.clip(r, -8, 7)
-        zero = np.full((N, K // group_size), 8, dtype=np.uint8)
-        codes = (q + 8).astype(np.uint8)
+        q = np.clip(r, -half, half - 1)
+        zero = np.full((N, K // group_size), SYM_ZERO, dtype=np.uint8)
+        codes = (q + SYM_ZERO).astype(np.uint8)
         clamped = q != r
     else:
         hi = np.maximum(np.max(grp, axis=2), 0.0)
         lo = np.minimum(np.min(grp, axis=2), 0.0)
         rng_ = fl32(hi - lo).astype(np.float64)
-        step = fl32(rng_ / QMAX_ASYM).astype(np.float64)
+        step = fl32(rng_ / qmax).astype(np.float64)
         step[step == 0.0] = 1.0
-        z = np.clip(np.rint(fl32(-lo / step).astype(np.float64)), 0, QMAX_ASYM)
+        z = np.clip(np.rint(fl32(-lo / step).astype(np.float64)), 0, qmax)
         r = np.rint(fl32(grp / step[:, :, None]).astype(np.float64)) + z[:, :, None]
-        q = np.clip(r, 0, QMAX_ASYM)
+        q = np.clip(r, 0, qmax)
         zero = z.astype(np.uint8)
         codes = q.astype(np.uint8)
         clamped = q != r
@@ -162,10 +171,10 @@ def unpack_nibbles(qweight: np.ndarray) -> np.ndarray:
 
 
 def quantize_pack(W: np.ndarray, s=None, group_size: int = 128,
-                  symmetric: bool = False) -> dict:
+                  symmetric: bool = False, bits: int = 4) -> dict:
     """The stored form: ``qweight`` [N, K/8] uint32, ``scales`` [K/G, N] fp16,
     ``zeros`` [K/G, N] uint8 (all 8 in symmetric mode), plus the :func:`quantize` details."""
-    qd = quantize(W, s, group_size, symmetric)
+    qd = quantize(W, s, group_size, symmetric, bits)
     qd["qweight"] = pack_nibbles(qd["codes"])
     qd["scales"] = np.ascontiguousarray(qd["step16"].T)
     qd["zeros"] = np.ascontiguousarray(qd["zero"].T)
@@ -208,7 +217,8 @@ def output_mse(X: np.ndarray, W: np.ndarray, W_hat: np.ndarray) -> float:
 
 
 def search_scale(W: np.ndarray, X: np.ndarray, alphas, group_size: int = 128,
-                 symmetric: bool = False, m=None, s_grid=None, eps: float = EPS) -> dict:
+                 symmetric: bool = False, m=None, s_grid=None, eps: float = EPS,
+                 bits: int = 4) -> dict:
     """The alpha search of one linear layer.
 
     For each alpha_i: s = max(m, eps)^alpha_i (rounded to fp32, the kernel's precision), codes of
@@ -224,7 +234,7 @@ def search_scale(W: np.ndarray, X: np.ndarray, alphas, group_size: int = 128,
     y = layer_output(X, W)
     err = np.zeros(len(s_grid), dtype=np.float64)
     for i, s in enumerate(s_grid):
-        qd = quantize_pack(W, s, group_size, symmetric)
+        qd = quantize_pack(W, s, group_size, symmetric, bits)
         w_hat = dequantize(qd["qweight"], qd["scales"], qd["zeros"], group_size, s=s)
         err[i] = float(np.mean((y - layer_output(X, w_hat)) ** 2))
     best = int(np.argmin(err))           # numpy returns the first minimiser
@@ -239,11 +249,12 @@ def error_of_codes(X: np.ndarray, W: np.ndarray, qweight, scales, zeros, s,
     return output_mse(X, W, w_hat)
 
 
-def residual(W: np.ndarray, s, group_size: int = 128, symmetric: bool = False) -> np.ndarray:
+def residual(W: np.ndarray, s, group_size: int = 128, symmetric: bool = False,
+             bits: int = 4) -> np.ndarray:
     """D = W - Q(W diag(s)) diag(s)^-1 in fp64: the weight error of one candidate, whose product
     with the calibration inputs is that candidate's output error, since
     W x - Q(W diag(s)) diag(s)^-1 x = D x ("AWQ Math", "Searching the scale")."""
-    qd = quantize_pack(W, s, group_size, symmetric)
+    qd = quantize_pack(W, s, group_size, symmetric, bits)
     w_hat = dequantize(qd["qweight"], qd["scales"], qd["zeros"], group_size, s=s)
     return np.asarray(W, dtype=np.float64) - w_hat
 

@@ -36,7 +36,8 @@ class AwqError(RuntimeError):
 
 
 class QCfg(ctypes.Structure):
-    _fields_ = [("group_size", ctypes.c_int32), ("symmetric", ctypes.c_int32)]
+    _fields_ = [("group_size", ctypes.c_int32), ("symmetric", ctypes.c_int32),
+                ("bits", ctypes.c_int32)]
 
 
 _c_void_p, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
@@ -116,8 +117,8 @@ def _stream(s):
     return int(s.cuda_stream)
 
 
-def _cfg(group_size=128, symmetric=False) -> QCfg:
-    return QCfg(int(group_size), 1 if symmetric else 0)
+def _cfg(group_size=128, symmetric=False, bits=4) -> QCfg:
+    return QCfg(int(group_size), 1 if symmetric else 0, int(bits))
 
 
 def _check(fn, status):
@@ -132,50 +133,53 @@ def awq_calib_stats(X, T, K, ldx, mean_abs, stream=None):
                                                     _stream(stream)))
 
 
-def awq_search_workspace_bytes(N, K, T, n_alpha, group_size=128, symmetric=False) -> int:
-    return int(lib().awq_search_workspace_bytes(N, K, T, n_alpha, _cfg(group_size, symmetric)))
+def awq_search_workspace_bytes(N, K, T, n_alpha, group_size=128, symmetric=False, bits=4) -> int:
+    return int(lib().awq_search_workspace_bytes(N, K, T, n_alpha,
+                                                _cfg(group_size, symmetric, bits)))
 
 
 def awq_search_scale(W, N, K, X, T, mean_abs, alphas, n_alpha, group_size, symmetric, workspace,
-                     ws_bytes, err_out, best_idx, s_out, inv_s_out, stream=None):
+                     ws_bytes, err_out, best_idx, s_out, inv_s_out, stream=None, bits=4):
     arr = (ctypes.c_float * int(n_alpha))(*[float(a) for a in alphas])
     _check("awq_search_scale", lib().awq_search_scale(
         _ptr(W), N, K, _ptr(X), T, _ptr(mean_abs), ctypes.cast(arr, ctypes.c_void_p), n_alpha,
-        _cfg(group_size, symmetric), _ptr(workspace), ws_bytes, _ptr(err_out), _ptr(best_idx),
+        _cfg(group_size, symmetric, bits), _ptr(workspace), ws_bytes, _ptr(err_out), _ptr(best_idx),
         _ptr(s_out), _ptr(inv_s_out), _stream(stream)))
 
 
 def awq_search_scale_static(W, N, K, X, T, mean_abs, alphas, n_alpha, group_size, symmetric,
-                            err_out, best_idx, s_out, inv_s_out, stream=None):
+                            err_out, best_idx, s_out, inv_s_out, stream=None, bits=4):
     """The alpha search with the library's static scratch array instead of a workspace, for
     callers that cannot allocate device memory (see include/awq.h). Allocates nothing."""
     arr = (ctypes.c_float * int(n_alpha))(*[float(a) for a in alphas])
     _check("awq_search_scale_static", lib().awq_search_scale_static(
         _ptr(W), N, K, _ptr(X), T, _ptr(mean_abs), ctypes.cast(arr, ctypes.c_void_p), n_alpha,
-        _cfg(group_size, symmetric), _ptr(err_out), _ptr(best_idx), _ptr(s_out),
+        _cfg(group_size, symmetric, bits), _ptr(err_out), _ptr(best_idx), _ptr(s_out),
         _ptr(inv_s_out), _stream(stream)))
 
 
 SEARCH_STATIC_SCRATCH_BYTES = 40 * 1024 * 1024
 
 
-def awq_quantize_pack(W, N, K, s, group_size, symmetric, qweight, scales, zeros, stream=None):
+def awq_quantize_pack(W, N, K, s, group_size, symmetric, qweight, scales, zeros, stream=None,
+                      bits=4):
     _check("awq_quantize_pack", lib().awq_quantize_pack(
-        _ptr(W), N, K, _ptr(s), _cfg(group_size, symmetric), _ptr(qweight), _ptr(scales),
+        _ptr(W), N, K, _ptr(s), _cfg(group_size, symmetric, bits), _ptr(qweight), _ptr(scales),
         _ptr(zeros), _stream(stream)))
 
 
-def awq_quant_residual(W, N, K, s, inv_s, group_size, symmetric, absmax_bits, D, stream=None):
+def awq_quant_residual(W, N, K, s, inv_s, group_size, symmetric, absmax_bits, D, stream=None,
+                       bits=4):
     _check("awq_quant_residual", lib().awq_quant_residual(
-        _ptr(W), N, K, _ptr(s), _ptr(inv_s), _cfg(group_size, symmetric), _ptr(absmax_bits),
+        _ptr(W), N, K, _ptr(s), _ptr(inv_s), _cfg(group_size, symmetric, bits), _ptr(absmax_bits),
         _ptr(D), _stream(stream)))
 
 
 def awq_w4a16_gemm(X, M, N, K, qweight, scales, zeros, inv_s, group_size, symmetric, Y,
-                   stream=None):
+                   stream=None, bits=4):
     _check("awq_w4a16_gemm", lib().awq_w4a16_gemm(
         _ptr(X), M, N, K, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s),
-        _cfg(group_size, symmetric), _ptr(Y), _stream(stream)))
+        _cfg(group_size, symmetric, bits), _ptr(Y), _stream(stream)))
 
 
 def awq_scale_rows(A, rows, cols, lda, row_scale, stream=None):
@@ -239,36 +243,37 @@ def calib_stats(X, stream=None):
     return m
 
 
-def quantize_pack(W, s=None, group_size=128, symmetric=False, stream=None):
-    """(qweight [N, K/8] int32, scales [K/G, N] fp16, zeros [K/G, N] uint8) of W diag(s)."""
+def quantize_pack(W, s=None, group_size=128, symmetric=False, stream=None, bits=4):
+    """(qweight [N, K/8] int32, scales [K/G, N] fp16, zeros [K/G, N] uint8) of W diag(s), with
+    ``bits``-wide codes in the 4-bit nibbles."""
     import torch
     N, K = W.shape
     q = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
     sc = torch.empty((K // group_size, N), dtype=torch.float16, device=W.device)
     z = torch.empty((K // group_size, N), dtype=torch.uint8, device=W.device)
-    awq_quantize_pack(W, N, K, s, group_size, symmetric, q, sc, z, stream)
+    awq_quantize_pack(W, N, K, s, group_size, symmetric, q, sc, z, stream, bits)
     return q, sc, z
 
 
-def quant_residual(W, s, inv_s, group_size=128, symmetric=False, stream=None):
+def quant_residual(W, s, inv_s, group_size=128, symmetric=False, stream=None, bits=4):
     """(D [N, K] fp16, absmax_bits [1] int32): D = 2^p (W - Q(W diag(s)) diag(s)^-1), p from
     max|W| whose fp32 bits absmax_bits holds (see awq_quant_residual)."""
     import torch
     N, K = W.shape
     D = torch.empty((N, K), dtype=torch.float16, device=W.device)
-    bits = torch.empty(1, dtype=torch.int32, device=W.device)
-    awq_quant_residual(W, N, K, s, inv_s, group_size, symmetric, bits, D, stream)
-    return D, bits
+    mx = torch.empty(1, dtype=torch.int32, device=W.device)
+    awq_quant_residual(W, N, K, s, inv_s, group_size, symmetric, mx, D, stream, bits)
+    return D, mx
 
 
 def search_scale(W, X, alphas, group_size=128, symmetric=False, mean_abs=None, workspace=None,
-                 stream=None):
+                 stream=None, bits=4):
     """The alpha search: returns (err [n] fp32, best_idx [1] int32, s [K], inv_s [K])."""
     import torch
     N, K = W.shape
     T = X.shape[0]
     n = len(alphas)
-    ws_bytes = awq_search_workspace_bytes(N, K, T, n, group_size, symmetric)
+    ws_bytes = awq_search_workspace_bytes(N, K, T, n, group_size, symmetric, bits)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=W.device)
     err = torch.empty(n, dtype=torch.float32, device=W.device)
@@ -276,7 +281,7 @@ def search_scale(W, X, alphas, group_size=128, symmetric=False, mean_abs=None, w
     s = torch.empty(K, dtype=torch.float32, device=W.device)
     inv_s = torch.empty(K, dtype=torch.float32, device=W.device)
     awq_search_scale(W, N, K, X, T, mean_abs, alphas, n, group_size, symmetric, workspace,
-                     workspace.numel(), err, best, s, inv_s, stream)
+                     workspace.numel(), err, best, s, inv_s, stream, bits)
     return err, best, s, inv_s
 
 

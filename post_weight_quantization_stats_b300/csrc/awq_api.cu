@@ -117,8 +117,12 @@ awq_status_t check_cfg(awq_qcfg_t cfg) {
   if (cfg.group_size != 32 && cfg.group_size != 64 && cfg.group_size != 128)
     return AWQ_ERR_INVALID_ARG;
   if (cfg.symmetric != 0 && cfg.symmetric != 1) return AWQ_ERR_INVALID_ARG;
+  if (cfg.bits != 0 && cfg.bits != 2 && cfg.bits != 3 && cfg.bits != 4) return AWQ_ERR_INVALID_ARG;
   return AWQ_OK;
 }
+
+// Code width of a validated configuration (0 means the default, 4).
+int cfg_bits(awq_qcfg_t cfg) { return cfg.bits == 0 ? 4 : cfg.bits; }
 
 constexpr int64_t kMaxElems = (int64_t{1} << 31) - 1;
 
@@ -261,7 +265,7 @@ awq_status_t launch_quantize_pack(const __half* W, int64_t N, int64_t K, const f
                                   awq_qcfg_t cfg, uint32_t* q, __half* scales, uint8_t* zeros,
                                   cudaStream_t st) {
   QuantArgs a{W, s, q, scales, cfg.symmetric ? nullptr : zeros, static_cast<int>(N),
-              static_cast<int>(K), cfg.symmetric};
+              static_cast<int>(K), cfg.symmetric, cfg_bits(cfg)};
   const dim3 grid(static_cast<unsigned>((N + 8 * QROWS - 1) / (8 * QROWS)),
                   static_cast<unsigned>((K / 8 + 31) / 32));
   prof_start(AWQ_K_QUANTIZE_PACK, st);
@@ -553,8 +557,8 @@ awq_status_t launch_search_persistent(int G, DeviceInfo* d, const SearchLayout& 
                                       __half* const* Dbuf, const __half* W,
                                       const unsigned int* absmax, const float* s_grid,
                                       const float* inv_grid, double* partial, int64_t N,
-                                      int64_t K, int n_alpha, int symmetric, bool* done,
-                                      cudaStream_t st);
+                                      int64_t K, int n_alpha, int symmetric, int bits,
+                                      bool* done, cudaStream_t st);
 
 // The schedule a search with `ws_bytes` of workspace takes (ws_bytes = SIZE_MAX: the one the
 // library prefers). Returns false if the workspace is too small.
@@ -583,8 +587,8 @@ awq_status_t launch_search_persistent(int G, DeviceInfo* d, const SearchLayout& 
                                       __half* const* Dbuf, const __half* W,
                                       const unsigned int* absmax, const float* s_grid,
                                       const float* inv_grid, double* partial, int64_t N,
-                                      int64_t K, int n_alpha, int symmetric, bool* done,
-                                      cudaStream_t st) {
+                                      int64_t K, int n_alpha, int symmetric, int bits,
+                                      bool* done, cudaStream_t st) {
   *done = false;
   CUtensorMap mXa, mXb, mD0, mD1, mB;
   AWQ_TRY(make_map(&mXa, Xt, K, L.Tp, L.Tp, gram::BM));
@@ -605,7 +609,7 @@ awq_status_t launch_search_persistent(int G, DeviceInfo* d, const SearchLayout& 
   sp.D[0] = Dbuf[0];
   sp.D[1] = Dbuf[1];
   sp.res = ResidualArgs{W, nullptr, nullptr, absmax, nullptr, static_cast<int>(N),
-                        static_cast<int>(K), symmetric};
+                        static_cast<int>(K), symmetric, bits};
   sp.s_grid = s_grid;
   sp.inv_grid = inv_grid;
   sp.partial = partial;
@@ -832,7 +836,7 @@ awq_status_t awq_quant_residual(const void* W_f16, int64_t N, int64_t K, const f
   absmax_kernel<<<agrid, 256, 0, st>>>(W, n8, absmax_bits);
   AWQ_TRY(launched(AWQ_K_ABSMAX, st));
   const ResidualArgs ra{W, s, inv_s, absmax_bits, static_cast<__half*>(D_f16),
-                        static_cast<int>(N), static_cast<int>(K), cfg.symmetric};
+                        static_cast<int>(N), static_cast<int>(K), cfg.symmetric, cfg_bits(cfg)};
   const dim3 rgrid(static_cast<unsigned>((N + 8 * QROWS - 1) / (8 * QROWS)),
                    static_cast<unsigned>((K / 8 + 31) / 32));
   prof_start(AWQ_K_RESIDUAL, st);
@@ -1002,7 +1006,8 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   // the residual of candidate i into buffer i % 2
   auto res_args = [&](int i) {
     return ResidualArgs{W, s_grid + static_cast<size_t>(i) * K, inv_grid + static_cast<size_t>(i) * K,
-                        absmax, Dbuf[i & 1], static_cast<int>(N), static_cast<int>(K), cfg.symmetric};
+                        absmax, Dbuf[i & 1], static_cast<int>(N), static_cast<int>(K), cfg.symmetric,
+                        cfg_bits(cfg)};
   };
   if (use_gram) {
     if (cudaMemsetAsync(hmax, 0, sizeof(unsigned int), st) != cudaSuccess) {
@@ -1027,7 +1032,7 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
     if (score_mode != AWQ_SCORE_GRAM_LAUNCHES) {
       AWQ_TRY(launch_search_persistent(cfg.group_size, d, L, ws, Xt, Bm, hmax, Dbuf, W, absmax,
                                        s_grid, inv_grid, partial, N, K, n_alpha, cfg.symmetric,
-                                       &persistent, st));
+                                       cfg_bits(cfg), &persistent, st));
     }
   }
   if (use_gram && !persistent) {

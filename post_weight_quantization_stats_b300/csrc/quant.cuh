@@ -1,10 +1,12 @@
-// Group-wise 4-bit quantiser of W diag(s) and the kernels built on it.
+// Group-wise N-bit quantiser of W diag(s) and the kernels built on it.
 //
 // "AWQ Math", "Weight-only quantization and where it breaks": Q(w) = step * round(w / step)
-// with step = max|w| / 2^(N-1) (the symmetric variant, codes clamped to [-8, 7] so 4 bits
-// hold them). "Shapes, granularity, and complexity" and "AWQ > Benefits and Practical
-// Considerations": one step and one zero point per group of input channels (asymmetric
-// variant: the group range widened to hold 0, step = (hi - lo) / 15, z = rint(-lo / step)).
+// with step = max|w| / 2^(N-1) for N-bit codes (the symmetric variant, codes clamped to
+// [-2^(N-1), 2^(N-1) - 1] and stored as q + 8). "Shapes, granularity, and complexity" and
+// "AWQ > Benefits and Practical Considerations": one step and one zero point per group of input
+// channels (asymmetric variant: the group range widened to hold 0, step = (hi - lo) / (2^N - 1),
+// z = rint(-lo / step)). N is 4 by default, 3 or 2 for the narrower variants; every width is
+// stored in 4-bit nibbles.
 //
 // Every operation that decides a code is an IEEE fp32 operation written as an intrinsic
 // (__fmul_rn, __fsub_rn, __fdiv_rn, rintf), so nothing is contracted into an FMA and the codes
@@ -24,13 +26,17 @@ struct GroupParams {
   float step;  // fp32 step the codes are decided with
   float zero;  // zero point as a float (exact small integer)
   float rcp;   // 1 / step, correctly rounded
+  float clo;   // smallest and largest stored code: 0 and 2^N - 1, or 8 -+ 2^(N-1) (symmetric)
+  float chi;
 };
 
-__device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric);
+__device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric,
+                                                      int bits);
 
 // Group step and zero point; TEAM = G / 8 consecutive lanes hold one group.
 template <int TEAM>
-__device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool symmetric) {
+__device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool symmetric,
+                                                    int bits) {
   float lo = wp[0], hi = wp[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) {
@@ -42,7 +48,7 @@ __device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool s
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
-  return group_params_of(lo, hi, symmetric);
+  return group_params_of(lo, hi, symmetric, bits);
 }
 
 // Round to the nearest integer, ties to even, for |x| < 2^22: x + 1.5 * 2^23 lies in a binade
@@ -52,33 +58,41 @@ __device__ __forceinline__ float rint_small(float x) {
   return __fsub_rn(__fadd_rn(x, 0x1.8p23f), 0x1.8p23f);
 }
 
-// fl32(d / 15) for d >= 0 without a division: q0 = fl32(d * r15) with r15 = fl32(1/15), the
-// remainder e = d - 15 q0 (exact in one FMA), and one correction q0 + e r15 rounded once
-// (Markstein's correction step, "IA-64 and Elementary Functions", 2000). The result is the
-// correctly rounded quotient for every d whose quotient is a normal float: the rounding
-// pattern of d / 15 depends only on d's significand, and all 2^23 significands were checked
-// against exact rational arithmetic. Smaller d take the IEEE division.
-__device__ __forceinline__ float div15(float d) {
-  constexpr float r15 = 0x1.111112p-4f;
-  if (d < 0x1p-100f) return __fdiv_rn(d, 15.0f);
-  const float q0 = __fmul_rn(d, r15);
-  return __fmaf_rn(__fmaf_rn(-q0, 15.0f, d), r15, q0);
+// fl32(d / n) for d >= 0 and n = 2^bits - 1 (15, 7 or 3) without a division: q0 = fl32(d * r)
+// with r = fl32(1/n), the remainder e = d - n q0 (exact in one FMA), and one correction
+// q0 + e r rounded once (Markstein's correction step, "IA-64 and Elementary Functions", 2000).
+// The result is the correctly rounded quotient for every d whose quotient is a normal float:
+// the rounding pattern of d / n depends only on d's significand, and all 2^23 significands were
+// checked against exact rational arithmetic for each n. Smaller d take the IEEE division.
+__device__ __forceinline__ float div_levels(float d, int bits) {
+  const float n = bits == 4 ? 15.0f : (bits == 3 ? 7.0f : 3.0f);
+  const float r = bits == 4 ? 0x1.111112p-4f : (bits == 3 ? 0x1.24924ap-3f : 0x1.555556p-2f);
+  if (d < 0x1p-100f) return __fdiv_rn(d, n);
+  const float q0 = __fmul_rn(d, r);
+  return __fmaf_rn(__fmaf_rn(-q0, n, d), r, q0);
 }
 
-// Step, zero point and reciprocal of a group from the min and max of its w'.
-__device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric) {
+// Step, zero point, reciprocal and code range of a group from the min and max of its w'.
+__device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric,
+                                                      int bits) {
   GroupParams g;
   if (symmetric) {
+    const float half = bits == 4 ? 8.0f : (bits == 3 ? 4.0f : 2.0f);  // 2^(N-1)
     const float amax = fmaxf(hi, -lo);  // max |w'| of the group
-    float st = __fmul_rn(amax, 0.125f);  // = fl32(amax / 8): the same exact value, rounded once
+    // fl32(amax / 2^(N-1)) as a multiplication by the exact power of two: the same value,
+    // rounded once
+    float st = __fmul_rn(amax, bits == 4 ? 0.125f : (bits == 3 ? 0.25f : 0.5f));
     if (st == 0.0f) st = 1.0f;
     g.step = st;
     g.zero = 8.0f;
     g.rcp = __frcp_rn(st);
+    g.clo = 8.0f - half;
+    g.chi = 7.0f + half;
   } else {
+    const float qmax = bits == 4 ? 15.0f : (bits == 3 ? 7.0f : 3.0f);  // 2^N - 1
     hi = fmaxf(hi, 0.0f);
     lo = fminf(lo, 0.0f);
-    float st = div15(__fsub_rn(hi, lo));
+    float st = div_levels(__fsub_rn(hi, lo), bits);
     if (st == 0.0f) st = 1.0f;
     g.step = st;
     g.rcp = __frcp_rn(st);
@@ -86,7 +100,9 @@ __device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool 
     const float t = __fmul_rn(-lo, g.rcp);
     float z = rint_small(t);
     if (fabsf(__fsub_rn(t, z)) >= 0.5f - 0x1p-17f) z = rintf(__fdiv_rn(-lo, st));
-    g.zero = fminf(fmaxf(z, 0.0f), 15.0f);
+    g.zero = fminf(fmaxf(z, 0.0f), qmax);
+    g.clo = 0.0f;
+    g.chi = qmax;
   }
   return g;
 }
@@ -105,17 +121,17 @@ __device__ __forceinline__ float rint_quotient(float wp, const GroupParams& g) {
   return r;
 }
 
-// Stored code (0..15) of one scaled weight, as an exact float.
-__device__ __forceinline__ float code_f(float wp, const GroupParams& g, bool symmetric) {
+// Stored code of one scaled weight, as an exact float: clamp(rint(w' / step) + zero) to the
+// code range (symmetric: zero = 8, so the clamp of q to [-2^(N-1), 2^(N-1) - 1] is shifted by 8).
+__device__ __forceinline__ float code_f(float wp, const GroupParams& g) {
   const float r = rint_quotient(wp, g);
-  if (symmetric) return __fadd_rn(fminf(fmaxf(r, -8.0f), 7.0f), 8.0f);
-  return fminf(fmaxf(__fadd_rn(r, g.zero), 0.0f), 15.0f);
+  return fminf(fmaxf(__fadd_rn(r, g.zero), g.clo), g.chi);
 }
 
 // The same code as an integer: the low bits of fl32(code + 2^23), whose unit in the last
 // place is 1 (no float-to-integer conversion instruction).
-__device__ __forceinline__ uint32_t code_of(float wp, const GroupParams& g, bool symmetric) {
-  return __float_as_uint(__fadd_rn(code_f(wp, g, symmetric), 0x1p23f)) & 0xFu;
+__device__ __forceinline__ uint32_t code_of(float wp, const GroupParams& g) {
+  return __float_as_uint(__fadd_rn(code_f(wp, g), 0x1p23f)) & 0xFu;
 }
 
 // ------------------------------------------------------------------ quantize + pack kernel
@@ -127,6 +143,7 @@ struct QuantArgs {
   __half* scales;       // [K/G, N]
   uint8_t* zeros;       // [K/G, N] or nullptr
   int N, K, symmetric;
+  int bits;             // code width: 4, 3 or 2
 };
 
 // Row-tiled launch shape shared by quantize_pack_kernel and residual_kernel: a block of 8 warps
@@ -185,11 +202,11 @@ __global__ void __launch_bounds__(256) quantize_pack_kernel(QuantArgs a) {
     unpack8(raw[r], wv);
 #pragma unroll
     for (int i = 0; i < 8; ++i) wp[i] = a.s ? __fmul_rn(wv[i], sv[i]) : wv[i];
-    const GroupParams g = group_params<TEAM>(wp, sym);   // every lane takes part in the shuffles
+    const GroupParams g = group_params<TEAM>(wp, sym, a.bits);  // every lane shuffles
     if (wok && row < a.N) {
       uint32_t packed = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) packed |= code_of(wp[i], g, sym) << (4 * i);
+      for (int i = 0; i < 8; ++i) packed |= code_of(wp[i], g) << (4 * i);
       a.qweight[static_cast<long long>(row) * kw + w] = packed;
       if ((lane & (TEAM - 1)) == 0) {
         const long long gi = static_cast<long long>(k0 / G) * a.N + row;
@@ -268,6 +285,7 @@ struct ResidualArgs {
   const unsigned int* absmax;  // max |W| bits
   __half* D;                   // [N, K] out: 2^p (W - Q(W diag(s)) diag(s)^-1)
   int N, K, symmetric;
+  int bits;                    // code width: 4, 3 or 2
 };
 
 // Residual of one alpha candidate: D = W - w_hat with w_hat = (q - z) * step16 / s, the
@@ -342,7 +360,7 @@ __device__ __forceinline__ void residual_rows(const ResidualArgs& a, const Resid
   }
   GroupParams g[RB];
 #pragma unroll
-  for (int q = 0; q < RB; ++q) g[q] = group_params_of(lo[q], hi[q], sym);
+  for (int q = 0; q < RB; ++q) g[q] = group_params_of(lo[q], hi[q], sym, a.bits);
   // The integers are carried shifted by kM = 1.5 * 2^23, where the unit in the last place is 1:
   // u = fl32(w' rcp + kM) = kM + rint(w' rcp) in one FMA, and kM - u = -rint(w' rcp) exactly,
   // so fma(w', rcp, kM - u) is w' rcp - rint(w' rcp) rounded once. Where that lies within
@@ -374,8 +392,8 @@ __device__ __forceinline__ void residual_rows(const ResidualArgs& a, const Resid
   for (int q = 0; q < RB; ++q) {
     const int row = r.rbase + q0 + q;
     // kM + (code - zero), clamped as code_f clamps the code (exact small integers plus kM)
-    const float ulo = __fadd_rn(kM, sym ? -8.0f : -g[q].zero);
-    const float uhi = __fadd_rn(kM, sym ? 7.0f : __fsub_rn(15.0f, g[q].zero));
+    const float ulo = __fadd_rn(kM, __fsub_rn(g[q].clo, g[q].zero));
+    const float uhi = __fadd_rn(kM, __fsub_rn(g[q].chi, g[q].zero));
     // With sp = step16 p2 (p2 a power of two, so exact): fma(u, sp, -kM sp) = (code - zero) sp
     // exactly (an integer below 16 times an 11-bit significand), times 1/s rounded once is
     // fl32((code - zero) step16 / s) p2 = w_hat p2, and fma(w, p2, -w_hat p2) =

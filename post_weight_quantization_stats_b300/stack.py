@@ -43,16 +43,18 @@ def read_manifest(out_dir: str) -> dict:
     return done
 
 
-def gpu_quantizer(alphas, group_size=128, symmetric=False):
-    """Statistic, alpha search and pack of one layer through libawq; returns host arrays."""
+def gpu_quantizer(alphas, group_size=128, symmetric=False, bits=4):
+    """Statistic, alpha search and pack of one layer through libawq (``bits``-wide codes);
+    returns host arrays."""
     import torch
 
     from . import awq
 
     def run(W, X):
         m = awq.calib_stats(X)
-        err, best, s, inv_s = awq.search_scale(W, X, alphas, group_size, symmetric, mean_abs=m)
-        q, sc, z = awq.quantize_pack(W, s, group_size, symmetric)
+        err, best, s, inv_s = awq.search_scale(W, X, alphas, group_size, symmetric, mean_abs=m,
+                                               bits=bits)
+        q, sc, z = awq.quantize_pack(W, s, group_size, symmetric, bits=bits)
         awq.awq_stream_status()
         torch.cuda.synchronize()
         return {"best": int(best.item()), "err": err.cpu().numpy(), "m": m.cpu().numpy(),

@@ -160,6 +160,50 @@ def pin_quant_nearest_level(o):
         assert np.all(chosen <= best + step * 2.0 ** -22), sym
 
 
+def pin_quant_bit_widths(o):
+    """N = 3 and N = 2 ("Weight-only quantization": D = max|w| / 2^(N-1) for N bits): exact
+    ladders of 2^N levels give their own indices as codes; the symmetric step is max|w| / 4 and
+    max|w| / 2, the top level clamps to 2^(N-1) - 1; every unclamped weight is within D/2; the
+    chosen code is a nearest of the 2^N representable levels; N = 4 is the default."""
+    G = 64
+    for bits in (3, 2):
+        n = 2 ** bits
+        d = 2.0 ** -5
+        for shift in (0, n // 2 - 1):                  # zero point 0 and mid-range
+            g = np.array([((i % n) - shift) * d for i in range(G)])
+            qd = o.quantize(g[None, :].astype(np.float16), None, G, False, bits)
+            assert qd["step32"][0, 0] == np.float32(d) and qd["zero"][0, 0] == shift
+            assert np.array_equal(qd["codes"][0], np.arange(G) % n)
+        h = n // 2
+        g = np.array([((i % (n + 1)) - h) * d for i in range(G)])   # -h .. +h steps
+        qd = o.quantize(g[None, :].astype(np.float16), None, G, True, bits)
+        assert qd["step32"][0, 0] == np.float32(h * d / h) and qd["zero"][0, 0] == 8
+        q = np.minimum((np.arange(G) % (n + 1)) - h, h - 1)
+        assert np.array_equal(qd["codes"][0].astype(int), q + 8)
+        assert np.array_equal(qd["clamped"][0], (np.arange(G) % (n + 1)) == n)
+        W, s = _bound_cases()
+        for sym in (False, True):
+            qd = o.quantize(W, s, 128, sym, bits)
+            wp = qd["scaled"]
+            g_of_k = np.arange(W.shape[1]) // 128
+            step = qd["step32"].astype(np.float64)[:, g_of_k]
+            zero = qd["zero"].astype(np.float64)[:, g_of_k]
+            c = qd["codes"].astype(np.int64)
+            lo_c, hi_c = (8 - h, 7 + h) if sym else (0, n - 1)
+            assert c.min() >= lo_c and c.max() <= hi_c
+            ok = ~qd["clamped"]
+            err = np.abs(wp - (c - zero) * step)
+            assert np.all(err[ok] <= step[ok] / 2 * (1 + 2.0 ** -20)), (bits, sym)
+            levels = (np.arange(lo_c, hi_c + 1)[None, None, :] - zero[:, :, None]) * step[:, :, None]
+            dist = np.abs(wp[:, :, None] - levels)
+            chosen = np.take_along_axis(dist, (c - lo_c)[:, :, None], 2)[:, :, 0]
+            assert np.all(chosen <= dist.min(axis=2) + step * 2.0 ** -22), (bits, sym)
+    W, s = _bound_cases()
+    for sym in (False, True):
+        a, b = o.quantize(W, s, 64, sym), o.quantize(W, s, 64, sym, 4)
+        assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["step32"], b["step32"])
+
+
 def pin_quant_equivariance(o):
     """A power-of-two scale of the whole weight scales the step and leaves codes unchanged."""
     W, _ = _bound_cases()

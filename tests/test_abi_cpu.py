@@ -104,6 +104,10 @@ def test_host_validation_rejects_without_cuda(L):
         S["AWQ_ERR_UNSUPPORTED_SHAPE"]
     assert _code(L, "awq_quantize_pack", A, 16, 256, None, awq.QCfg(48, 0), A, A, A, None) == \
         S["AWQ_ERR_INVALID_ARG"]
+    for bad_bits in (1, 5, 8, -1):                        # code widths: 0 (= 4), 2, 3, 4
+        assert _code(L, "awq_quantize_pack", A, 16, 256, None, awq.QCfg(128, 0, bad_bits), A, A,
+                     A, None) == S["AWQ_ERR_INVALID_ARG"]
+        assert awq.lib().awq_search_workspace_bytes(16, 256, 8, 2, awq.QCfg(128, 0, bad_bits)) == 0
     assert _code(L, "awq_quantize_pack", A, 16, 256, None, cfg, A, A, None, None) == \
         S["AWQ_ERR_INVALID_ARG"]                          # asymmetric needs zeros
     assert _code(L, "awq_quantize_pack", A, 16, 256, A + 4, cfg, A, A, A, None) == \
@@ -146,6 +150,9 @@ def test_valid_call_without_a_gpu_reports_no_device(L):
         awq.STATUS_CODE["AWQ_ERR_NO_DEVICE"]
     assert _code(L, "awq_quant_residual", A, 16, 256, A, A, cfg, A, A, None) == \
         awq.STATUS_CODE["AWQ_ERR_NO_DEVICE"]
+    for bits in (2, 3, 4):                                # accepted: only the device check fails
+        assert _code(L, "awq_quantize_pack", A, 16, 256, None, awq.QCfg(128, 1, bits), A, A, A,
+                     None) == awq.STATUS_CODE["AWQ_ERR_NO_DEVICE"]
 
 
 def test_launch_counter_starts_without_launches(L):

@@ -90,6 +90,28 @@ def test_quantize_pack_bitexact(N, K, G, sym, with_s):
         assert np.array_equal(host(z), want["zeros"])
 
 
+@pytest.mark.parametrize("bits", [3, 2])
+@pytest.mark.parametrize("G", [32, 64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_quantize_pack_narrow_codes_bitexact(bits, G, sym):
+    """3- and 2-bit codes (step = max|w'| / 2^(N-1) symmetric, (hi - lo) / (2^N - 1)
+    asymmetric), stored in the 4-bit nibbles: codes, steps and zero points bit-exact."""
+    for N, K in ((300, 1152), (7, 128), (64, 4096)):
+        d = layer(N + K + G + bits, N, K, 4)
+        rng = np.random.Generator(np.random.PCG64(N + bits))
+        s = np.exp(rng.uniform(-2, 3, K)).astype(np.float32)
+        for ss in (None, s):
+            q, sc, z = awq.quantize_pack(dev(d["W"]), dev(ss) if ss is not None else None, G, sym,
+                                         bits=bits)
+            awq.awq_stream_status()
+            want = ref.quantize_pack(d["W"], ss, G, sym, bits)
+            assert np.array_equal(host(q).view(np.uint32), want["qweight"])
+            assert np.array_equal(host(sc), want["scales"])
+            if not sym:
+                assert np.array_equal(host(z), want["zeros"])
+                assert int(host(z).max()) <= 2 ** bits - 1
+
+
 def test_quantize_pack_special_groups():
     """All-zero, all-positive, all-negative and constant groups, and exact half-way codes."""
     K = 256
@@ -129,7 +151,7 @@ def test_quantize_pack_full_size_sampled_rows():
 
 # ----------------------------------------------------------------------------- search
 
-def _score_bound(X16, W16, s_grid, G, sym):
+def _score_bound(X16, W16, s_grid, G, sym, bits=4):
     """Per-alpha bound on |E_gpu - E_exact| from the GPU's arithmetic: the residual D is rounded
     to fp16 after a power-of-two scale (relative error <= 2^-11, absolute <= 2^-25 2^-p in the
     subnormal range) and accumulated in fp32 over K products (<= K 2^-24 relative of sum |x D|).
@@ -142,7 +164,7 @@ def _score_bound(X16, W16, s_grid, G, sym):
     p = 14 - e
     out = []
     for s in s_grid:
-        qd = ref.quantize_pack(W16, s, G, sym)
+        qd = ref.quantize_pack(W16, s, G, sym, bits)
         D = W16.astype(np.float64) - ref.dequantize(qd["qweight"], qd["scales"], qd["zeros"], G, s=s)
         y = X @ D.T
         b = (2.0 ** -11 + K * 2.0 ** -23) * (np.abs(X) @ np.abs(D).T) \
@@ -151,7 +173,7 @@ def _score_bound(X16, W16, s_grid, G, sym):
     return np.array(out)
 
 
-def _gram_bound(X16, W16, s_grid, G, sym):
+def _gram_bound(X16, W16, s_grid, G, sym, bits=4):
     """Per-alpha bound on |E_gram - E_exact| for the Gram schedule: D rounded to fp16
     (2 * 2^-11 of |d|^T A |d|, A = |X|^T |X| >= |H|), H accumulated in fp32 over T tokens
     (T 2^-24), rounded to fp16 (2^-11), and d^T H' d accumulated in fp32 over K + 256 terms; so
@@ -162,7 +184,7 @@ def _gram_bound(X16, W16, s_grid, G, sym):
     c = 3 * 2.0 ** -11 + (K + T + 256) * 2.0 ** -23
     out = []
     for s in s_grid:
-        qd = ref.quantize_pack(W16, s, G, sym)
+        qd = ref.quantize_pack(W16, s, G, sym, bits)
         D = W16.astype(np.float64) - ref.dequantize(qd["qweight"], qd["scales"], qd["zeros"], G, s=s)
         out.append(c * float(np.sum((X @ np.abs(D).T) ** 2)) / (T * W16.shape[0]))
     return np.array(out)
@@ -177,20 +199,20 @@ def score_mode(mode):
         awq.awq_set_score_mode("auto")
 
 
-def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False, gram=False):
+def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False, gram=False, bits=4):
     W, X = dev(W16), dev(X16)
     m = awq.calib_stats(X) if use_m else None
-    err, best, s, inv_s = awq.search_scale(W, X, alphas, G, sym, mean_abs=m)
+    err, best, s, inv_s = awq.search_scale(W, X, alphas, G, sym, mean_abs=m, bits=bits)
     awq.awq_stream_status()
     m_gpu = host(awq.calib_stats(X))
-    r = ref.search_scale(W16, X16, alphas, G, sym, m=m_gpu)
+    r = ref.search_scale(W16, X16, alphas, G, sym, m=m_gpu, bits=bits)
     e = host(err).astype(np.float64)
     small = X16.shape[0] * W16.shape[0] < 4096
     bound = 0.0
     if small:
-        bound = _score_bound(X16, W16, r["s_grid"], G, sym)
+        bound = _score_bound(X16, W16, r["s_grid"], G, sym, bits)
         if gram:
-            bound = bound + _gram_bound(X16, W16, r["s_grid"], G, sym)
+            bound = bound + _gram_bound(X16, W16, r["s_grid"], G, sym, bits)
     tol = np.maximum(1e-3 * r["err"], bound)
     assert np.all(np.abs(e - r["err"]) <= tol), (e, r["err"], tol)
     b = int(host(best)[0])
@@ -211,18 +233,18 @@ def _ulp16(x):
     return 2.0 ** (np.floor(np.log2(m)) - 10)
 
 
-def _check_residual(W, s, G, sym):
+def _check_residual(W, s, G, sym, bits=4):
     """The GPU's 2^p (W - w_hat) against the oracle's fp64 residual: within one fp16 spacing
     plus the fp32 roundings of w_hat and of the difference (2^-21 |w_hat| scaled). A code that
     differs from the oracle's moves D by a whole step, and a tie broken the other way flips the
     sign of a half step: both far outside that bound. max|W| comes back bit-exact."""
     inv = (np.float32(1) / s).astype(np.float32)
-    D, bits = awq.quant_residual(dev(W), dev(s), dev(inv), G, sym)
+    D, mbits = awq.quant_residual(dev(W), dev(s), dev(inv), G, sym, bits=bits)
     awq.awq_stream_status()
     mx = np.float32(np.max(np.abs(W.astype(np.float32))))
-    assert host(bits).view(np.uint32)[0] == mx.view(np.uint32)
+    assert host(mbits).view(np.uint32)[0] == mx.view(np.uint32)
     p = ref.residual_exponent(W)
-    qd = ref.quantize_pack(W, s, G, sym)
+    qd = ref.quantize_pack(W, s, G, sym, bits)
     w_hat = ref.dequantize(qd["qweight"], qd["scales"], qd["zeros"], G, s=s)
     exact = (W.astype(np.float64) - w_hat) * 2.0 ** p
     got = host(D).astype(np.float64)
@@ -240,6 +262,15 @@ def test_quant_residual_matches_oracle(N, K, G, sym):
     W = synth.draw_weight(rng, N, K, 0.02)
     s = np.exp(rng.uniform(-3.0, 3.0, K)).astype(np.float32)
     _check_residual(W, s, G, sym)
+
+
+@pytest.mark.parametrize("bits", [3, 2])
+@pytest.mark.parametrize("G,sym", [(128, False), (64, True), (32, False)])
+def test_quant_residual_narrow_codes(bits, G, sym):
+    rng = np.random.Generator(np.random.PCG64(G + bits))
+    W = synth.draw_weight(rng, 200, 1024, 0.02)
+    s = np.exp(rng.uniform(-3.0, 3.0, 1024)).astype(np.float32)
+    _check_residual(W, s, G, sym, bits)
 
 
 def test_quant_residual_special_groups():
@@ -275,6 +306,20 @@ def test_quant_residual_near_ties_full_size():
     for a in (0.35, 0.8):
         s = ref.fl32(ref.scale_grid(m, [a]))[0].astype(np.float32)
         _check_residual(W, s, 128, False)
+
+
+@pytest.mark.parametrize("bits", [3, 2])
+@pytest.mark.parametrize("mode", ["gram", "direct"])
+def test_search_narrow_codes(bits, mode):
+    """The alpha search with 3- and 2-bit codes, both score forms, against the oracle's search
+    at the same width; narrower codes make every candidate's error larger."""
+    d = layer(5 + bits, 256, 512, 300, n_out=5)
+    alphas = synth.alpha_grid(20)
+    with score_mode(mode):
+        e, b, r = _check_search(d["W"], d["X"], alphas, 128, False, gram=(mode == "gram"),
+                                bits=bits)
+        e4, _, _ = _check_search(d["W"], d["X"], alphas, 128, False, gram=(mode == "gram"))
+    assert np.all(e > e4)
 
 
 def test_search_tiny_layer():
@@ -427,12 +472,12 @@ def test_search_full_size_llama7b_attn():
 
 # ----------------------------------------------------------------------------- W4A16 matmul
 
-def _gemm_case(N, K, M, G, sym, with_inv, seed):
+def _gemm_case(N, K, M, G, sym, with_inv, seed, bits=4):
     d = layer(seed, N, K, M, n_out=max(1, K // 64), mult=4.0)
     W16, X16 = d["W"], d["X"]
     rng = np.random.Generator(np.random.PCG64(seed + 1))
     s = np.exp(rng.uniform(-0.5, 1.0, K)).astype(np.float32)
-    qd = ref.quantize_pack(W16, s, G, sym)
+    qd = ref.quantize_pack(W16, s, G, sym, bits)
     inv = (np.float32(1) / s).astype(np.float32) if with_inv else None
     q = dev(qd["qweight"].view(np.int32))
     Y = awq.w4a16_gemm(dev(X16), q, dev(qd["scales"]), dev(qd["zeros"]),
@@ -460,6 +505,13 @@ def test_w4a16_shapes(N, K, M, G, sym, with_inv):
     if K % G:
         pytest.skip("K % G")
     _gemm_case(N, K, M, G, sym, with_inv, N * 7 + K + M)
+
+
+@pytest.mark.parametrize("M", [1, 2, 16, 128])
+@pytest.mark.parametrize("bits,sym", [(3, False), (3, True), (2, False)])
+def test_w4a16_narrow_codes(M, bits, sym):
+    """3- and 2-bit codes in the 4-bit nibbles go through every matmul kernel unchanged."""
+    _gemm_case(300, 1152, M, 128, sym, True, 7 * M + bits, bits)
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 16, 17, 200])

@@ -1,12 +1,15 @@
 """Host-side proofs of the arithmetic shortcuts the quantising kernels rely on (no GPU).
 
-The group step of the asymmetric quantiser is fl32((hi - lo) / 15). The kernels form it without
-a division: q0 = fl32(d * r15) with r15 = fl32(1/15), the remainder e = d - 15 q0 (exact, one
-FMA), and q1 = fl32(q0 + e * r15) (one FMA), Markstein's correction step. Whether that equals
-the correctly rounded quotient depends only on d's significand (scaling d by 2^j scales every
-quantity by 2^j while the results stay normal), so checking all 2^23 significands of one binade
-with exact integer arithmetic proves it for every d whose quotient is a normal float.
+The group step of the asymmetric quantiser is fl32((hi - lo) / n) with n = 2^N - 1 levels (15,
+7 or 3 for 4-, 3- and 2-bit codes). The kernels form it without a division: q0 = fl32(d * r)
+with r = fl32(1/n), the remainder e = d - n q0 (exact, one FMA), and q1 = fl32(q0 + e * r) (one
+FMA), Markstein's correction step. Whether that equals the correctly rounded quotient depends
+only on d's significand (scaling d by 2^j scales every quantity by 2^j while the results stay
+normal), so checking all 2^23 significands of one binade with exact integer arithmetic proves
+it for every d whose quotient is a normal float.
 """
+
+import pytest
 
 from fractions import Fraction
 
@@ -37,32 +40,40 @@ def _rn32(fr: Fraction) -> Fraction:
     return f * ulp
 
 
-def test_division_by_15_with_one_correction_is_correctly_rounded():
-    r15 = np.float32(1) / np.float32(15)
-    assert float(r15).hex() == "0x1.1111120000000p-4"            # the kernel's constant
-    R = int(float(r15) * 2.0 ** 27)                                # r15 = R 2^-27, R < 2^24
-    assert R * 2.0 ** -27 == float(r15) and 2 ** 23 <= R < 2 ** 24
+KERNEL_RECIPROCALS = {15: "0x1.1111120000000p-4", 7: "0x1.24924a0000000p-3",
+                      3: "0x1.5555560000000p-2"}
+
+
+@pytest.mark.parametrize("n", [15, 7, 3])
+def test_division_by_levels_with_one_correction_is_correctly_rounded(n):
+    r = np.float32(1) / np.float32(n)
+    assert float(r).hex() == KERNEL_RECIPROCALS[n]                  # the kernel's constant
+    _, er = np.frexp(float(r))                                     # r in [2^(er-1), 2^er)
+    sr = 24 - int(er)                                              # r = R 2^-sr, R < 2^24
+    R = int(float(r) * 2.0 ** sr)
+    assert R * 2.0 ** -sr == float(r) and 2 ** 23 <= R < 2 ** 24
+    u = 23 + sr                                                    # unit 2^-u for d r and e
     X = np.arange(2 ** 23, 2 ** 24, dtype=np.int64)                # d = X 2^-23 in [1, 2)
-    P = X * R                                                      # d r15 = P 2^-50, exact
+    P = X * R                                                      # d r = P 2^-u, exact
     nb = np.floor(np.log2(P.astype(np.float64))).astype(np.int64)
     nb = np.where((np.int64(1) << (nb + 1)) <= P, nb + 1, nb)
     nb = np.where((np.int64(1) << nb) > P, nb - 1, nb)
     sh = nb - 23
-    Q0 = _rn_shift(P, sh)                                          # q0 = Q0 2^(sh - 50)
+    Q0 = _rn_shift(P, sh)                                          # q0 = Q0 2^(sh - u)
     carry = Q0 >= (np.int64(1) << 24)
     Q0 = np.where(carry, Q0 >> 1, Q0)
     sh = np.where(carry, sh + 1, sh)
-    E = (X << 27) - 15 * (Q0 << sh)                                # e = E 2^-50, exact
-    C = E * R                                                      # e r15 = C 2^-77
-    lsb = sh + 27                                                  # q0's ulp = 2^lsb units
+    E = (X << sr) - n * (Q0 << sh)                                 # e = E 2^-u, exact
+    C = E * R                                                      # e r = C 2^-(u + sr)
+    lsb = sh + sr                                                  # q0's ulp = 2^lsb units
     k = C >> lsb
     rem = C - (k << lsb)
     half = np.int64(1) << (lsb - 1)
     Q1 = Q0 + k + ((rem > half) | ((rem == half) & (((Q0 + k) & 1) == 1)))
-    num = X << (27 - sh)                                           # d / 15 in q0's ulps = num / 15
-    kq = num // 15
-    rq = num - kq * 15
-    Qc = kq + ((2 * rq > 15) | ((2 * rq == 15) & ((kq & 1) == 1)))
+    num = X << (sr - sh)                                           # d / n in q0's ulps = num / n
+    kq = num // n
+    rq = num - kq * n
+    Qc = kq + ((2 * rq > n) | ((2 * rq == n) & ((kq & 1) == 1)))
     # the correction changes the answer where the plain product is wrong ...
     assert np.count_nonzero(Q0 != Qc) > 10 ** 6
     # ... and is right for every significand (a quotient that lands on a binade edge is checked
@@ -70,8 +81,8 @@ def test_division_by_15_with_one_correction_is_correctly_rounded():
     edge = (Q1 >= (1 << 24)) | (Q1 < (1 << 23)) | (Qc >= (1 << 24))
     assert np.count_nonzero(edge) < 100
     assert np.array_equal(Q1[~edge], Qc[~edge])
-    rf = Fraction(float(r15))
+    rf = Fraction(float(r))
     for i in np.nonzero(edge)[0]:
         d = Fraction(int(X[i]), 2 ** 23)
         q0 = _rn32(d * rf)
-        assert _rn32(q0 + (d - 15 * q0) * rf) == _rn32(d / 15)
+        assert _rn32(q0 + (d - n * q0) * rf) == _rn32(d / n)

@@ -16,15 +16,15 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), 
                    "awq_ref.py")
 
 MUTATIONS = {
-    "range divisor 16 instead of 15": ("rng_ / QMAX_ASYM", "rng_ / 16"),
+    "range divisor 16 instead of 15": ("rng_ / qmax", "rng_ / (qmax + 1)"),
     "zero point sign flipped": ("np.rint(fl32(-lo / step)", "np.rint(fl32(lo / step)"),
     "zero point added with wrong sign": ("grp / step[:, :, None]).astype(np.float64)) + z",
                                          "grp / step[:, :, None]).astype(np.float64)) - z"),
     "floor instead of round": ("r = np.rint(fl32(grp", "r = np.floor(fl32(grp"),
     "range not widened to hold 0": ("hi = np.maximum(np.max(grp, axis=2), 0.0)",
                                     "hi = np.max(grp, axis=2)"),
-    "symmetric divisor 7": ("fl32(amax / SYM_DIV)", "fl32(amax / 7.0)"),
-    "symmetric clamp [-7, 7]": ("np.clip(r, -8, 7)", "np.clip(r, -7, 7)"),
+    "symmetric divisor 7": ("fl32(amax / half)", "fl32(amax / (half - 1))"),
+    "symmetric clamp [-7, 7]": ("np.clip(r, -half, half - 1)", "np.clip(r, -half + 1, half - 1)"),
     "scaled weight divides by s": ("fl32(W64 * s32[None, :])", "fl32(W64 / s32[None, :])"),
     "dequant multiplies by s": ("w_hat = w_hat / np.asarray(s", "w_hat = w_hat * np.asarray(s"),
     "dequant adds the zero point": ("(codes - zero[:, g_of_k])", "(codes + zero[:, g_of_k])"),
@@ -36,6 +36,8 @@ MUTATIONS = {
     "residual adds the dequantised weight": ("np.asarray(W, dtype=np.float64) - w_hat",
                                              "np.asarray(W, dtype=np.float64) + w_hat"),
     "residual exponent off by one": ("return 14 - int(e)", "return 15 - int(e)"),
+    "asymmetric levels fixed at 16": ("qmax = 2 ** bits - 1", "qmax = 15"),
+    "symmetric half-range fixed at 8": ("half = 2 ** (bits - 1)", "half = 8"),
     "statistic drops the absolute value": ("total += np.abs(X64[t])", "total += X64[t]"),
     "statistic divides by T - 1": ("return total / T", "return total / (T - 1)"),
     "statistic uses the max": ("total += np.abs(X64[t])",
