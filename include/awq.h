@@ -10,9 +10,10 @@
  *                      group-wise to 4 bits; E(alpha) = mean over tokens and outputs of
  *                      (W x - Q(W') diag(s)^-1 x)^2; alpha* = the first minimiser
  *                      ("AWQ Math", "The equivalent transform", "Searching the scale")
- *   awq_quantize_pack  4-bit codes of W diag(s), one step and one zero point per group of
- *                      input channels ("AWQ Math", "Weight-only quantization and where it
- *                      breaks" and "Shapes, granularity, and complexity")
+ *   awq_quantize_pack  4-bit codes of W diag(s) (3- or 2-bit codes with cfg.bits, in the same
+ *                      nibbles), one step and one zero point per group of input channels
+ *                      ("AWQ Math", "Weight-only quantization and where it breaks" and
+ *                      "Shapes, granularity, and complexity")
  *   awq_w4a16_gemm     Y = X (dequant(Q) diag(inv_s))^T without materialising fp16 weights
  *                      ("AWQ > Benefits and Practical Considerations": unpack the 4-bit
  *                      integers, apply the group scale and zero point and, optionally, the
