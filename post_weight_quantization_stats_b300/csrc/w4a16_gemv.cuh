@@ -12,18 +12,22 @@
 //
 // The consumers are P x RG warps: part p of K (IPL items of 32 channels per lane, 1024 * IPL
 // channels per warp) times row group rg. A lane's activations never change: the CTA stages
-// x~ = x * inv_s once in shared memory with coalesced loads, and each lane copies its K slice
-// into registers; afterwards the only shared-memory traffic per code is the bulk copy's write
-// and one 16-byte read per item. Per
-// item and row:
-//   * codes become exact (q - z) half2 pairs by the 0x6400 fp16 exponent trick (q + 1024 sits
-//     in the mantissa of a half in [1024, 2048));
-//   * HFMA2 multiplies them into x~ / 64 (a power of two: exact unless subnormal) in two
-//     accumulators of 8 products per half, so partial sums stay below 120 |x~| / 64 and
-//     cannot overflow for any |x~| below 34,000;
-//   * the item sum is scaled by 64 * step and accumulated in fp32.
-// Row partials are reduced with shuffles and written to shared memory per (row, part); the
-// parts are added in a fixed order at the end, so the result is deterministic.
+// x~ = fp16(x * inv_s) (what the folded activation would be) once in shared memory as 16-bit
+// block fixed point, x~ = x_int 2^(e - 15) with one exponent e per 32 channels (max|x~| < 2^e,
+// so |x_int| < 2^15; exact for every x~ within 2^5 of the block's maximum, rounded to the
+// nearest integer below that), split into a low byte plane (0..255) and a signed high byte
+// plane (x_int = 256 hi + lo), and each lane copies its K slice into registers. Afterwards the
+// only shared-memory traffic per code is the bulk copy's write and one 16-byte read per item.
+// Per item and row:
+//   * the 8 codes of a word become two words of 4 bytes (even and odd nibbles: one AND, one
+//     shift-and-AND);
+//   * four DP4A integer dot products (codes x low plane unsigned, codes x high plane signed)
+//     accumulate sum q x_int exactly in 32-bit integers;
+//   * the zero point comes off as z * sum x_int (staged per item), and the exact integer is
+//     scaled by step * 2^(e - 15) into an fp32 row accumulator.
+// So the only roundings are the fixed point of small activations and the fp32 accumulation
+// over items. Row partials are reduced with shuffles and written to shared memory per (row,
+// part); the parts are added in a fixed order at the end, so the result is deterministic.
 //
 // Launched with programmatic dependent launch: the kernel lets the next W4A16 launch of the
 // stream start right after its own set-up, and it streams its weights and stages its group
@@ -44,7 +48,6 @@ constexpr int ITEM_CH = 32;               // channels of one lane item (4 packed
 constexpr int MAX_M = 2;
 constexpr int MAX_STAGES = 8;
 constexpr int SMEM_BUDGET = 220 * 1024;
-constexpr float X_PRESCALE = 1.0f / 64.0f;
 
 // Items per lane for M tokens: the registers holding x~ stay at 64 per thread.
 __host__ __device__ constexpr int items_per_lane(int M) { return M == 1 ? 4 : 2; }
@@ -73,34 +76,30 @@ __host__ __device__ inline int ysum_floats(const Args& a) {
   return (a.rows_max * a.parts * a.M + 3) & ~3;
 }
 __host__ __device__ inline int param_words(const Args& a) { return (a.rows_max * a.pstride + 3) & ~3; }
+// x planes: 16 words per (token, 32-channel item), i.e. 2 bytes per activation
 __host__ __device__ inline size_t xs_bytes(const Args& a) {
   return static_cast<size_t>(a.M) * static_cast<size_t>(a.K) * 2;
 }
+// per (token, item): sum of x_int (int) and 2^(e - 15) (float)
+__host__ __device__ inline size_t xitem_bytes(const Args& a) {
+  return static_cast<size_t>(a.M) * static_cast<size_t>(a.K / ITEM_CH) * 8;
+}
 __host__ __device__ inline size_t smem_bytes(const Args& a) {
-  return static_cast<size_t>(a.nstages) * a.stage_bytes + xs_bytes(a) +
+  return static_cast<size_t>(a.nstages) * a.stage_bytes + xs_bytes(a) + xitem_bytes(a) +
          static_cast<size_t>(param_words(a)) * 4 + static_cast<size_t>(ysum_floats(a)) * 4 +
          2 * MAX_STAGES * 8 + 16;
 }
 
-// 8 codes of one word -> 4 exact half2 (q - z) pairs in the order (0,4), (1,5), (2,6), (3,7).
-// zsub = 1024 + z (subtracted from the low-nibble lanes), zadd = -(64 + z) (added to the
-// x/16 high-nibble lanes).
-__device__ __forceinline__ void unpack_qz(uint32_t w, __half2 zsub, __half2 zadd, __half2 (&o)[4]) {
-  const uint32_t t0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);        // 1024 + q0 | q4
-  const uint32_t t1 = lop3_and_or(w, 0x00F000F0u, 0x64006400u);        // 1024 + 16 q1 | q5
-  const uint32_t w8 = w >> 8;
-  const uint32_t t2 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);       // 1024 + q2 | q6
-  const uint32_t t3 = lop3_and_or(w8, 0x00F000F0u, 0x64006400u);       // 1024 + 16 q3 | q7
-  const __half2 sixteenth = __float2half2_rn(0.0625f);
-  o[0] = __hsub2(*reinterpret_cast<const __half2*>(&t0), zsub);
-  o[1] = __hfma2(*reinterpret_cast<const __half2*>(&t1), sixteenth, zadd);
-  o[2] = __hsub2(*reinterpret_cast<const __half2*>(&t2), zsub);
-  o[3] = __hfma2(*reinterpret_cast<const __half2*>(&t3), sixteenth, zadd);
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  return __dp4a(a, b, c);
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }
 
-// Group parameters of every row of the CTA, as half2 (step, 1024 + z), row-major with a padded
-// row stride (pstride = K / G + 1) so neither the staging writes nor the per-item reads
-// conflict on banks.
+// Group parameters of every row of the CTA, one word each: the fp16 step in the low half and
+// the zero point in bits 16..23, row-major with a padded row stride (pstride = K / G + 1) so
+// neither the staging writes nor the per-item reads conflict on banks.
 template <int G>
 __device__ __forceinline__ void stage_params(const Args& a, uint32_t* prm, int r0, int nrows) {
   const int ng = a.K / G;
@@ -108,40 +107,73 @@ __device__ __forceinline__ void stage_params(const Args& a, uint32_t* prm, int r
     const int g = idx / nrows, rl = idx - (idx / nrows) * nrows;
     const long long gi = static_cast<long long>(g) * a.N + r0 + rl;
     const __half st = a.scales[gi];
-    const float z = a.zeros ? static_cast<float>(a.zeros[gi]) : 8.0f;
-    const __half2 v = __halves2half2(st, __float2half_rn(1024.0f + z));
-    prm[rl * a.pstride + g] = *reinterpret_cast<const uint32_t*>(&v);
+    const uint32_t z = a.zeros ? static_cast<uint32_t>(a.zeros[gi]) : 8u;
+    prm[rl * a.pstride + g] = static_cast<uint32_t>(__half_as_ushort(st)) | (z << 16);
   }
 }
 
-// x~ / 64 of every token, staged once per CTA with coalesced 16-byte loads: slot j (channels
-// 8j .. 8j+7) of token m holds the pair order (x0,x4), (x1,x5), (x2,x6), (x3,x7). fp16(x * inv_s)
-// is what the folded activation would be; the 2^-6 prescale is exact on it.
+// x~ of every token as 16-bit block fixed point, staged once per CTA. Slot s (token m, item
+// it, word w: channels 32 it + 8 w .. + 7) goes to consumer thread s mod CTHREADS, so the four
+// words of an item sit on four consecutive lanes. A lane rounds x * inv_s of its 8 channels to
+// fp16; the four lanes take the item's max|x~| (a max over the float bits, which order like the
+// values for |x~|) and e with max|x~| < 2^e; each lane forms x_int = rint(x~ 2^(15 - e)) and
+// packs its word's four byte planes with byte permutes: the low bytes of channels 8w + 0, 2, 4,
+// 6 (even nibbles), of 8w + 1, 3, 5, 7 (odd nibbles), then the signed high bytes in the same
+// two orders (x_int = 256 hi + lo). The item's sum of x_int and 2^(e - 15) go to xsum / xsc.
 template <int M>
-__device__ __forceinline__ void stage_x(const Args& a, uint4* xs) {
-  const int slots = a.K / 8;
-  for (int idx = threadIdx.x; idx < M * slots; idx += CTHREADS) {
-    const int m = idx / slots, j = idx - (idx / slots) * slots;
-    const int k = 8 * j;
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.X + static_cast<long long>(m) * a.K + k));
-    const __half* xv = reinterpret_cast<const __half*>(&raw);
+__device__ __forceinline__ void stage_x(const Args& a, uint32_t* xs, int* xsum, float* xsc) {
+  const int wpt = a.K / 8;                  // words (slots) per token
+  const int total = M * wpt;                // a multiple of 4: K is a multiple of 32
+  for (int s0 = threadIdx.x - (threadIdx.x & 31); s0 < total; s0 += CTHREADS) {
+    const int s = s0 + (threadIdx.x & 31);  // the loop bound is warp-uniform: shuffles below
+    const bool on = s < total;
+    const int m = on ? s / wpt : 0, k = on ? (s - m * wpt) * 8 : 0;
     float f[8];
-    if (a.inv_s) {
-      const float4 ia = __ldg(reinterpret_cast<const float4*>(a.inv_s + k));
-      const float4 ib = __ldg(reinterpret_cast<const float4*>(a.inv_s + k) + 1);
-      const float iv[8] = {ia.x, ia.y, ia.z, ia.w, ib.x, ib.y, ib.z, ib.w};
+    {
+      const uint4 raw = on ? __ldg(reinterpret_cast<const uint4*>(a.X + static_cast<long long>(m) * a.K + k))
+                           : make_uint4(0, 0, 0, 0);
+      const __half* xv = reinterpret_cast<const __half*>(&raw);
+      if (a.inv_s && on) {
+        const float4 ia = __ldg(reinterpret_cast<const float4*>(a.inv_s + k));
+        const float4 ib = __ldg(reinterpret_cast<const float4*>(a.inv_s + k) + 1);
+        const float iv[8] = {ia.x, ia.y, ia.z, ia.w, ib.x, ib.y, ib.z, ib.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = __half2float(xv[e]) * iv[e];
-    } else {
+        for (int e = 0; e < 8; ++e) f[e] = __half2float(__float2half_rn(__half2float(xv[e]) * iv[e]));
+      } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = __half2float(xv[e]);
+        for (int e = 0; e < 8; ++e) f[e] = __half2float(xv[e]);
+      }
     }
-    __align__(16) __half2 pr[4];
+    float mx = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      pr[e] = __halves2half2(__float2half_rn(__half2float(__float2half_rn(f[e])) * X_PRESCALE),
-                             __float2half_rn(__half2float(__float2half_rn(f[e + 4])) * X_PRESCALE));
-    xs[idx] = *reinterpret_cast<const uint4*>(pr);
+    for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(f[e]));
+    unsigned mb = __float_as_uint(mx);
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    int ex = 0;
+    frexpf(__uint_as_float(mb), &ex);       // max|x~| < 2^ex (0 for an all-zero item)
+    const float up = ldexpf(1.0f, 15 - ex);
+    int xi[8];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      xi[e] = __float2int_rn(f[e] * up);    // the product is exact (a power-of-two scale)
+      sum += xi[e];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if (on) {
+      // byte 0 (low) or 1 (high) of channels (0, 2) and (4, 6), or (1, 3) and (5, 7)
+      const uint32_t le = __byte_perm(__byte_perm(xi[0], xi[2], 0x0040), __byte_perm(xi[4], xi[6], 0x0040), 0x5410);
+      const uint32_t lo = __byte_perm(__byte_perm(xi[1], xi[3], 0x0040), __byte_perm(xi[5], xi[7], 0x0040), 0x5410);
+      const uint32_t he = __byte_perm(__byte_perm(xi[0], xi[2], 0x0051), __byte_perm(xi[4], xi[6], 0x0051), 0x5410);
+      const uint32_t ho = __byte_perm(__byte_perm(xi[1], xi[3], 0x0051), __byte_perm(xi[5], xi[7], 0x0051), 0x5410);
+      reinterpret_cast<uint4*>(xs)[s] = make_uint4(le, lo, he, ho);
+      if ((s & 3) == 0) {
+        xsum[s >> 2] = sum;
+        xsc[s >> 2] = ldexpf(1.0f, ex - 15);
+      }
+    }
   }
 }
 
@@ -150,8 +182,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
   constexpr int IPL = items_per_lane(M);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  uint4* xs = reinterpret_cast<uint4*>(smem + static_cast<size_t>(a.nstages) * a.stage_bytes);
-  uint32_t* prm = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(xs) + xs_bytes(a));
+  uint32_t* xs = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(a.nstages) * a.stage_bytes);
+  int* xsum = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(xs) + xs_bytes(a));
+  float* xsc = reinterpret_cast<float*>(xsum + M * (a.K / ITEM_CH));
+  uint32_t* prm = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(xs) + xs_bytes(a) +
+                                              xitem_bytes(a));
   float* ysum = reinterpret_cast<float*>(prm + param_words(a));
   uint64_t* full = reinterpret_cast<uint64_t*>(ysum + ysum_floats(a));
   uint64_t* empty = full + MAX_STAGES;
@@ -210,29 +245,36 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
   // Activations (and the output) may belong to the previous kernel of the stream: everything
   // below waits for it. The weight stream and the group parameters above do not.
   pdl_wait();
-  stage_x<M>(a, xs);
+  stage_x<M>(a, xs, xsum, xsc);
   named_bar_sync(1, CTHREADS);
-  // each lane's x~ slice: 4 consecutive 16-byte slots per item (conflict-free: a warp reads
-  // 32 consecutive items' slots in four passes)
-  __half2 xr[M][IPL][16];
+  // each lane's x planes (16 words per item: four 16-byte loads), the item's sum of x_int and
+  // its 2^(e - 15), kept in registers for the whole kernel
+  uint32_t xr[M][IPL][16];
+  int sx[M][IPL];
+  float sc[M][IPL];
   if (active) {
 #pragma unroll
     for (int u = 0; u < IPL; ++u) {
       const int it = part * IPL * 32 + lane + 32 * u;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
+        const bool ok_it = it < items;
+        const int xi = m * items + (ok_it ? it : 0);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const uint4 q = it < items ? xs[m * (a.K / 8) + it * 4 + v] : make_uint4(0, 0, 0, 0);
-          const __half2* h2 = reinterpret_cast<const __half2*>(&q);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) xr[m][u][v * 4 + e] = h2[e];
+          const uint4 q = ok_it ? reinterpret_cast<const uint4*>(xs)[xi * 4 + v]
+                                : make_uint4(0, 0, 0, 0);
+          xr[m][u][4 * v + 0] = q.x;
+          xr[m][u][4 * v + 1] = q.y;
+          xr[m][u][4 * v + 2] = q.z;
+          xr[m][u][4 * v + 3] = q.w;
         }
+        sx[m][u] = ok_it ? xsum[xi] : 0;
+        sc[m][u] = ok_it ? xsc[xi] : 0.0f;
       }
     }
   }
 
-  const __half2 c960 = __float2half2_rn(960.0f);
   bool ok = true;
   for (int j = 0; j < nstage_total; ++j) {
     const int s = j % a.nstages;
@@ -256,29 +298,29 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
           if (it < items) {
             const uint4 qv = *reinterpret_cast<const uint4*>(codes + it * 16);
             const uint32_t pw = prow[(it * ITEM_CH) / G];
-            const __half2 pv = *reinterpret_cast<const __half2*>(&pw);
-            const __half2 zsub = __high2half2(pv);                     // 1024 + z
-            const __half2 zadd = __hsub2(c960, zsub);             // -(64 + z), exact
-            const float step64 = __low2float(pv) * 64.0f;
+            const float step = __half2float(__ushort_as_half(static_cast<unsigned short>(pw & 0xFFFFu)));
+            const int z = static_cast<int>((pw >> 16) & 0xFFu);
             const uint32_t wq[4] = {qv.x, qv.y, qv.z, qv.w};
-            __half2 qz[16];
+            uint32_t ev[4], od[4];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              __half2 o[4];
-              unpack_qz(wq[v], zsub, zadd, o);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) qz[v * 4 + e] = o[e];
+              ev[v] = wq[v] & 0x0F0F0F0Fu;          // nibbles 0, 2, 4, 6 as bytes
+              od[v] = (wq[v] >> 4) & 0x0F0F0F0Fu;   // nibbles 1, 3, 5, 7
             }
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-              __half2 h0 = __float2half2_rn(0.f), h1 = h0;
+              uint32_t lo = 0u;
+              int hi = 0;
 #pragma unroll
-              for (int e = 0; e < 16; e += 2) {
-                h0 = __hfma2(qz[e], xr[m][u][e], h0);
-                h1 = __hfma2(qz[e + 1], xr[m][u][e + 1], h1);
+              for (int v = 0; v < 4; ++v) {
+                lo = dp4a_uu(ev[v], xr[m][u][4 * v + 0], lo);
+                lo = dp4a_uu(od[v], xr[m][u][4 * v + 1], lo);
+                hi = dp4a_ss(ev[v], xr[m][u][4 * v + 2], hi);
+                hi = dp4a_ss(od[v], xr[m][u][4 * v + 3], hi);
               }
-              const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-              acc[m] = fmaf((f0.x + f0.y) + (f1.x + f1.y), step64, acc[m]);
+              // sum (q - z) x_int, exact: |.| < 32 * 15 * 2^15 < 2^24, so the float is exact too
+              const int t = hi * 256 + static_cast<int>(lo) - z * sx[m][u];
+              acc[m] = fmaf(static_cast<float>(t), step * sc[m][u], acc[m]);
             }
           }
         }
