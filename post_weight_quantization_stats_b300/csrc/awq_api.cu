@@ -375,10 +375,19 @@ awq_status_t gemv_shape(gemv::Args& a, int G, int sms) {
   a.pstride = a.K / G + 1;
   // no more stages than the CTA's rows fill (at least 2)
   const int stages_needed = (a.rows_max + a.rows_stage - 1) / a.rows_stage;
-  a.nstages = std::max(2, std::min(gemv::MAX_STAGES, stages_needed));
-  while (a.nstages > 2 && gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) --a.nstages;
-  if (gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) return AWQ_ERR_UNSUPPORTED_SHAPE;
-  return AWQ_OK;
+  auto fit = [&]() {
+    a.nstages = std::max(2, std::min(gemv::MAX_STAGES, stages_needed));
+    while (a.nstages > 2 && gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) --a.nstages;
+    return gemv::smem_bytes(a) <= static_cast<size_t>(gemv::SMEM_BUDGET);
+  };
+  a.x_direct = 0;
+  if (fit()) return AWQ_OK;
+  // The staged activation planes do not fit beside two weight stages (long K with M = 2). With
+  // at most two row groups no two lanes of a CTA share activations, so each lane converts its
+  // own (measured slower where the staged form fits, hence only here).
+  if (a.row_groups > 2) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  a.x_direct = 1;
+  return fit() ? AWQ_OK : AWQ_ERR_UNSUPPORTED_SHAPE;
 }
 
 template <int M>

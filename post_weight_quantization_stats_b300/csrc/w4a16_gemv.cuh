@@ -67,6 +67,7 @@ struct Args {
   int nstages;            // ring depth, 2..MAX_STAGES
   int rows_max;           // max output rows of one CTA
   int pstride;            // words per CTA row of staged group parameters: K / G + 1
+  int x_direct;           // 1: each lane converts its own activations (no staged x planes)
   int* status;
   unsigned long long limit_ns;
 };
@@ -76,13 +77,14 @@ __host__ __device__ inline int ysum_floats(const Args& a) {
   return (a.rows_max * a.parts * a.M + 3) & ~3;
 }
 __host__ __device__ inline int param_words(const Args& a) { return (a.rows_max * a.pstride + 3) & ~3; }
-// x planes: 16 words per (token, 32-channel item), i.e. 2 bytes per activation
+// x planes: 16 words per (token, 32-channel item), i.e. 2 bytes per activation (none when each
+// lane converts its own)
 __host__ __device__ inline size_t xs_bytes(const Args& a) {
-  return static_cast<size_t>(a.M) * static_cast<size_t>(a.K) * 2;
+  return a.x_direct ? 0 : static_cast<size_t>(a.M) * static_cast<size_t>(a.K) * 2;
 }
 // per (token, item): sum of x_int (int) and 2^(e - 15) (float)
 __host__ __device__ inline size_t xitem_bytes(const Args& a) {
-  return static_cast<size_t>(a.M) * static_cast<size_t>(a.K / ITEM_CH) * 8;
+  return a.x_direct ? 0 : static_cast<size_t>(a.M) * static_cast<size_t>(a.K / ITEM_CH) * 8;
 }
 __host__ __device__ inline size_t smem_bytes(const Args& a) {
   return static_cast<size_t>(a.nstages) * a.stage_bytes + xs_bytes(a) + xitem_bytes(a) +
@@ -177,6 +179,63 @@ __device__ __forceinline__ void stage_x(const Args& a, uint32_t* xs, int* xsum, 
   }
 }
 
+// The same conversion done by one lane for one whole item it owns (long K: every lane's items
+// are its own, so nothing is shared and nothing staged): the 32 activations from global memory,
+// max|x~| and e within the lane, the four words' byte planes with byte permutes.
+__device__ __forceinline__ void convert_item(const Args& a, int m, int it, uint32_t (&planes)[16],
+                                             int& xsum_out, float& xsc_out) {
+  const int k0 = it * ITEM_CH;
+  __half2 h[16];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.X + static_cast<long long>(m) * a.K +
+                                                           k0 + 8 * v));
+    const __half* xv = reinterpret_cast<const __half*>(&raw);
+    float f[8];
+    if (a.inv_s) {
+      const float4 ia = __ldg(reinterpret_cast<const float4*>(a.inv_s + k0 + 8 * v));
+      const float4 ib = __ldg(reinterpret_cast<const float4*>(a.inv_s + k0 + 8 * v) + 1);
+      const float iv[8] = {ia.x, ia.y, ia.z, ia.w, ib.x, ib.y, ib.z, ib.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __half2float(xv[e]) * iv[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __half2float(xv[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      h[4 * v + e] = __halves2half2(__float2half_rn(f[2 * e]), __float2half_rn(f[2 * e + 1]));
+  }
+  float mx = 0.f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const float2 p = __half22float2(h[c]);
+    mx = fmaxf(mx, fmaxf(fabsf(p.x), fabsf(p.y)));
+  }
+  int ex = 0;
+  frexpf(mx, &ex);                          // max|x~| < 2^ex (0 for an all-zero item)
+  const float up = ldexpf(1.0f, 15 - ex);
+  int sum = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    int xi[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 p = __half22float2(h[4 * w + e]);
+      xi[2 * e] = __float2int_rn(p.x * up);      // the product is exact (a power-of-two scale)
+      xi[2 * e + 1] = __float2int_rn(p.y * up);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum += xi[e];
+    planes[4 * w + 0] = __byte_perm(__byte_perm(xi[0], xi[2], 0x0040), __byte_perm(xi[4], xi[6], 0x0040), 0x5410);
+    planes[4 * w + 1] = __byte_perm(__byte_perm(xi[1], xi[3], 0x0040), __byte_perm(xi[5], xi[7], 0x0040), 0x5410);
+    planes[4 * w + 2] = __byte_perm(__byte_perm(xi[0], xi[2], 0x0051), __byte_perm(xi[4], xi[6], 0x0051), 0x5410);
+    planes[4 * w + 3] = __byte_perm(__byte_perm(xi[1], xi[3], 0x0051), __byte_perm(xi[5], xi[7], 0x0051), 0x5410);
+  }
+  xsum_out = sum;
+  xsc_out = ldexpf(1.0f, ex - 15);
+}
+
 template <int M, int G>
 __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
   constexpr int IPL = items_per_lane(M);
@@ -245,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
   // Activations (and the output) may belong to the previous kernel of the stream: everything
   // below waits for it. The weight stream and the group parameters above do not.
   pdl_wait();
-  stage_x<M>(a, xs, xsum, xsc);
+  if (!a.x_direct) stage_x<M>(a, xs, xsum, xsc);
   named_bar_sync(1, CTHREADS);
   // each lane's x planes (16 words per item: four 16-byte loads), the item's sum of x_int and
   // its 2^(e - 15), kept in registers for the whole kernel
@@ -259,6 +318,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_kernel(Args a) {
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         const bool ok_it = it < items;
+        if (a.x_direct) {
+          if (ok_it) {
+            convert_item(a, m, it, xr[m][u], sx[m][u], sc[m][u]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) xr[m][u][v] = 0u;
+            sx[m][u] = 0;
+            sc[m][u] = 0.0f;
+          }
+          continue;
+        }
         const int xi = m * items + (ok_it ? it : 0);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {

@@ -549,6 +549,28 @@ def test_w4a16_full_size_sampled(M):
     assert np.max(np.abs(got - want)) / np.max(np.abs(want)) <= 2e-2
 
 
+@pytest.mark.parametrize("M", [1, 2])
+def test_w4a16_long_k_decode_sampled(M):
+    """28672 -> 8192 at M = 1 and 2: at M = 2 the staged activation planes do not fit beside the
+    weight ring, so each lane converts its own activations; 4096 sampled outputs against the
+    oracle."""
+    N, K = 8192, 28672
+    rng = np.random.Generator(np.random.PCG64(40 + M))
+    W16 = synth.draw_weight(rng, N, K, 0.01)
+    X16 = rng.standard_normal((M, K)).astype(np.float16)
+    s = np.exp(rng.uniform(-0.5, 1.0, K)).astype(np.float32)
+    q, sc, z = awq.quantize_pack(dev(W16), dev(s))
+    inv = (np.float32(1) / s).astype(np.float32)
+    Y = awq.w4a16_gemm(dev(X16), q, sc, z, dev(inv))
+    awq.awq_stream_status()
+    rows = rng.integers(0, M, 4096)
+    cols = rng.integers(0, N, 4096)
+    want = ref.w4a16_gemm_entries(X16, host(q).view(np.uint32), host(sc), host(z), rows, cols,
+                                  inv_s=inv)
+    got = host(Y)[rows, cols].astype(np.float64)
+    assert np.max(np.abs(got - want)) / np.max(np.abs(want)) <= 2e-2
+
+
 def test_w4a16_deterministic():
     d = layer(8, 512, 1024, 128)
     q, sc, z = awq.quantize_pack(dev(d["W"]))
