@@ -1,4 +1,6 @@
-"""Host-side proofs of the arithmetic shortcuts the quantising kernels rely on (no GPU).
+"""Host-side proofs of the arithmetic shortcuts the kernels rely on (no GPU): the division-free
+group step of the quantiser, and the integer form of the decode GEMV (byte planes and DP4A order,
+exactness of the 16-bit block fixed point).
 
 The group step of the asymmetric quantiser is fl32((hi - lo) / n) with n = 2^N - 1 levels (15,
 7 or 3 for 4-, 3- and 2-bit codes). The kernels form it without a division: q0 = fl32(d * r)
@@ -86,3 +88,60 @@ def test_division_by_levels_with_one_correction_is_correctly_rounded(n):
         d = Fraction(int(X[i]), 2 ** 23)
         q0 = _rn32(d * rf)
         assert _rn32(q0 + (d - n * q0) * rf) == _rn32(d / n)
+
+
+# ---------------------------------------------------------------- decode GEMV integer form
+
+def _byte_perm(x, y, s):
+    """PTX prmt (default mode): byte i of the result is byte (s >> 4i) & 7 of {y, x}."""
+    b = [(x >> (8 * i)) & 0xFF for i in range(4)] + [(y >> (8 * i)) & 0xFF for i in range(4)]
+    return sum(b[(s >> (4 * i)) & 7] << (8 * i) for i in range(4))
+
+
+def _planes(xi8):
+    """The four byte planes of one packed word (channels 8w .. 8w+7), as the kernel builds them."""
+    u = [int(v) & 0xFFFFFFFF for v in xi8]
+    le = _byte_perm(_byte_perm(u[0], u[2], 0x0040), _byte_perm(u[4], u[6], 0x0040), 0x5410)
+    lo = _byte_perm(_byte_perm(u[1], u[3], 0x0040), _byte_perm(u[5], u[7], 0x0040), 0x5410)
+    he = _byte_perm(_byte_perm(u[0], u[2], 0x0051), _byte_perm(u[4], u[6], 0x0051), 0x5410)
+    ho = _byte_perm(_byte_perm(u[1], u[3], 0x0051), _byte_perm(u[5], u[7], 0x0051), 0x5410)
+    return le, lo, he, ho
+
+
+def _dp4a(a, b, c, b_signed):
+    sb = [((b >> (8 * i)) & 0xFF) for i in range(4)]
+    if b_signed:
+        sb = [v - 256 if v >= 128 else v for v in sb]
+    return c + sum(((a >> (8 * i)) & 0xFF) * sb[i] for i in range(4))
+
+
+def test_gemv_byte_planes_give_the_exact_integer_dot():
+    """Codes of one 32-channel item (nibble i of word w is channel 8w + i) split into even and
+    odd nibble bytes, activations x_int in [-2^15, 2^15) split into the planes above: four DP4A
+    per word give sum q x_int, and hi * 256 + lo - z * sum x_int is sum (q - z) x_int exactly."""
+    rng = np.random.Generator(np.random.PCG64(5))
+    for _ in range(300):
+        xi = rng.integers(-32767, 32768, 32)
+        q = rng.integers(0, 16, 32)
+        z = int(rng.integers(0, 16))
+        lo = hi = 0
+        for w in range(4):
+            word = sum(int(q[8 * w + i]) << (4 * i) for i in range(8))
+            ev, od = word & 0x0F0F0F0F, (word >> 4) & 0x0F0F0F0F
+            le, lo_p, he, ho = _planes(xi[8 * w: 8 * w + 8])
+            lo = _dp4a(od, lo_p, _dp4a(ev, le, lo, False), False)
+            hi = _dp4a(od, ho, _dp4a(ev, he, hi, True), True)
+        assert hi * 256 + lo - z * int(xi.sum()) == int(((q - z) * xi).sum())
+
+
+def test_fixed_point_is_exact_within_five_binades_of_the_block_max():
+    """x~ = x_int 2^(e - 15) with max|x~| < 2^e: every fp16 x~ with |x~| >= 2^(e - 5) times
+    2^(15 - e) is an integer (its 11-bit significand ends at or above 2^(e - 15)), so only
+    smaller activations are rounded; and |x_int| stays below 2^15."""
+    h = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)   # finite >= 0
+    h = h[h > 0]
+    for e in range(-10, 17):
+        blk = h[h < 2.0 ** e]
+        big = blk[blk >= 2.0 ** (e - 5)]
+        scaled = big * 2.0 ** (15 - e)
+        assert np.all(scaled == np.rint(scaled)) and np.all(scaled < 2 ** 15)
