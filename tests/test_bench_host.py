@@ -87,3 +87,22 @@ def test_reference_arm_emits_contract_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 2
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_profiled_traffic_follows_every_kernel_source(tmp_path, monkeypatch):
+    """The roofline's `traffic` comes from a committed ncu summary only while the digest of all
+    the kernel's source files matches the one recorded with the counters: changing any of them
+    (not just the first) voids it."""
+    csrc = tmp_path / "post_weight_quantization_stats_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "a.cuh").write_text("kernel a\n")
+    (csrc / "b.cuh").write_text("helpers b\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.source_digest(("a.cuh", "b.cuh"))
+    (tmp_path / "profiles" / "k.md").write_text(
+        f"source_sha256_16: {sha}\n\n| traffic_bytes_per_launch | 12345 |\n")
+    assert bench.profiled_traffic("k.md", ("a.cuh", "b.cuh")) == 12345
+    (csrc / "b.cuh").write_text("helpers b, changed\n")
+    assert bench.profiled_traffic("k.md", ("a.cuh", "b.cuh")) is None
+    assert bench.profiled_traffic("k.md", ("a.cuh", "missing.cuh")) is None
