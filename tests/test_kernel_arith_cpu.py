@@ -145,3 +145,52 @@ def test_fixed_point_is_exact_within_five_binades_of_the_block_max():
         big = blk[blk >= 2.0 ** (e - 5)]
         scaled = big * 2.0 ** (15 - e)
         assert np.all(scaled == np.rint(scaled)) and np.all(scaled < 2 ** 15)
+
+
+# ---------------------------------------------------------------- residual code decisions
+
+def _rn32_signed(fr: Fraction) -> Fraction:
+    if fr == 0:
+        return Fraction(0)
+    return _rn32(fr) if fr > 0 else -_rn32(-fr)
+
+
+def _rint_even(fr: Fraction) -> int:
+    f = fr.numerator // fr.denominator
+    rem = fr - f
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and f % 2 == 1):
+        f += 1
+    return f
+
+
+def test_residual_shifted_domain_codes_equal_the_quotient_rule():
+    """The residual decides rint(fl32(w' / step)) as u = fl32(w' r + kM) (one FMA, kM = 1.5 2^23,
+    r = fl32(1 / step)), checks fl32(w' r + (kM - u)) against 1/2 - 2^-17, and takes the IEEE
+    quotient only past that margin. In exact arithmetic, on quotients concentrated near the
+    rounding boundaries, both give the same integer as the pack kernel's rule."""
+    kM = Fraction(3 * 2 ** 22)
+    margin = Fraction(1, 2) - Fraction(1, 2 ** 17)
+    rng = np.random.Generator(np.random.PCG64(9))
+    n_edge = n_fast_wrong = 0
+    for i in range(4000):
+        step = _rn32_signed(Fraction(float(np.float32(np.exp(rng.uniform(-9, 3))))))
+        k = int(rng.integers(-15, 16))
+        if i % 2:
+            q = Fraction(k) + Fraction(1, 2) + Fraction(int(rng.integers(-2 ** 12, 2 ** 12)), 2 ** 28)
+        else:
+            q = Fraction(float(rng.uniform(-15.4, 15.4)))
+        wp = _rn32_signed(q * step)                      # a representable w' near that quotient
+        want = _rint_even(_rn32_signed(wp / step))
+        r = _rn32_signed(1 / step)
+        u = _rn32_signed(wp * r + kM)
+        e = _rn32_signed(wp * r + (kM - u))
+        n_fast_wrong += int(u - kM) != want
+        if abs(e) >= margin:
+            n_edge += 1
+            got = _rint_even(_rn32_signed(wp / step))
+        else:
+            got = int(u - kM)
+        assert got == want, (float(wp), float(step))
+    # the near-boundary branch was exercised, and the samples reach quotients where the fast
+    # path alone would pick the wrong integer
+    assert n_edge > 0 and n_fast_wrong > 0
