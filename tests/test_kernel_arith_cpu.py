@@ -164,10 +164,11 @@ def _rint_even(fr: Fraction) -> int:
 
 
 def test_residual_shifted_domain_codes_equal_the_quotient_rule():
-    """The residual decides rint(fl32(w' / step)) as u = fl32(w' r + kM) (one FMA, kM = 1.5 2^23,
-    r = fl32(1 / step)), checks fl32(w' r + (kM - u)) against 1/2 - 2^-17, and takes the IEEE
-    quotient only past that margin. In exact arithmetic, on quotients concentrated near the
-    rounding boundaries, both give the same integer as the pack kernel's rule."""
+    """rint(fl32(w' / step)) without a division, both ways the kernels take it (r = fl32(1/step),
+    kM = 1.5 2^23): the pack kernel rounds t = fl32(w' r) with two adds against kM and checks
+    |t - rint(t)| against 1/2 - 2^-17; the residual forms u = fl32(w' r + kM) in one FMA and checks
+    fl32(w' r + (kM - u)). Past the margin both take the IEEE quotient. In exact arithmetic, on
+    quotients concentrated near the rounding boundaries, both give the defined integer."""
     kM = Fraction(3 * 2 ** 22)
     margin = Fraction(1, 2) - Fraction(1, 2 ** 17)
     rng = np.random.Generator(np.random.PCG64(9))
@@ -191,6 +192,11 @@ def test_residual_shifted_domain_codes_equal_the_quotient_rule():
         else:
             got = int(u - kM)
         assert got == want, (float(wp), float(step))
+        t = _rn32_signed(wp * r)                        # the pack kernel's rule
+        rt = _rn32_signed(_rn32_signed(t + kM) - kM)
+        got_pack = _rint_even(_rn32_signed(wp / step)) if abs(_rn32_signed(t - rt)) >= margin \
+            else int(rt)
+        assert got_pack == want, (float(wp), float(step))
     # the near-boundary branch was exercised, and the samples reach quotients where the fast
     # path alone would pick the wrong integer
     assert n_edge > 0 and n_fast_wrong > 0
