@@ -407,8 +407,9 @@ def pin_residual(o):
     Wb, sb = _bound_cases()
     for sym in (False, True):
         for gs in (64, 128):
-            Db = o.residual(Wb, sb, gs, sym)
-            assert np.all(np.abs(Db) <= np.abs(Wb.astype(np.float64)) * (1 + 2.0 ** -20))
+            for bits in (4, 3, 2):        # at every code width (the GPU's 2^p scale relies on it)
+                Db = o.residual(Wb, sb, gs, sym, bits)
+                assert np.all(np.abs(Db) <= np.abs(Wb.astype(np.float64)) * (1 + 2.0 ** -20))
     assert o.residual_exponent(W) == 14          # max|W| = 1/2 < 2^0
     assert o.residual_exponent(np.array([[1.0, -0.25]], np.float16)) == 13
     assert o.residual_exponent(np.array([[-65504.0]], np.float16)) == -2
