@@ -102,6 +102,8 @@ def source_digest(sources):
 def profiled_traffic(profile_md, sources):
     """DRAM bytes per launch from a committed ncu summary, or None when any source the kernel
     is built from has changed since the counters were taken (the digest no longer matches)."""
+    if profile_md is None:
+        return None
     path = os.path.join(ROOT, "profiles", profile_md)
     sha = source_digest(sources)
     if sha is None or not os.path.exists(path):
@@ -378,20 +380,72 @@ def choose_rows(layer, alphas, gemm_m, G, budget_s):
     return rows, d["m"]
 
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo), or None."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def oracle_single_thread(layer, s, G, budget_s=2.0):
+    """The oracle's statistic and quantise-pack on one thread (BLAS limited to one thread; the
+    numpy element-wise work is single-threaded anyway), on leading samples of the layer's X and
+    W: GB/s of the algorithmic bytes (2 T K for the statistic; 2 N K + 4 K + packed bytes for
+    the pack)."""
+    import contextlib
+
+    from oracle import awq_ref as ref
+    try:
+        from threadpoolctl import threadpool_limits
+        one_thread = threadpool_limits(1)
+    except Exception:  # noqa: BLE001
+        one_thread = contextlib.nullcontext()
+    with one_thread:
+        X, W = layer["X"], layer["W"]
+        K = X.shape[1]
+        t_rows = max(1, min(X.shape[0], int(2 ** 22 // K)))
+        t0 = time.perf_counter()
+        ref.calib_stats(X[:t_rows])
+        t_stats = time.perf_counter() - t0
+        n_rows = max(1, min(W.shape[0], int(2 ** 20 // K)))
+        t0 = time.perf_counter()
+        ref.quantize_pack(W[:n_rows], s, G)
+        t_pack = time.perf_counter() - t0
+    pack_bytes = 2 * n_rows * K + 4 * K + n_rows * K // 2 + 3 * n_rows * (K // G)
+    return {"threads": 1,
+            "calib_stats_gbs": round(2 * t_rows * K / t_stats / 1e9, 4),
+            "quantize_pack_gbs": round(pack_bytes / t_pack / 1e9, 4),
+            "sample": f"statistic over the first {t_rows} tokens, pack of the first {n_rows} "
+                      f"output rows (K={K})"}
+
+
 def cpu_baseline(layer, alphas, gemm_m, G, budget_s=12.0):
     rows, m = choose_rows(layer, alphas, gemm_m, G, budget_s)
     sec, d = oracle_layer_seconds(layer, alphas, gemm_m, G, rows)
     N, K = layer["W"].shape
     T = layer["X"].shape[0]
+    from oracle import awq_ref as ref
+    s = ref.fl32(ref.scale_grid(m, [0.5]))[0].astype(np.float32)
     return {"value": 1.0 / sec, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"oracle (fp64 numpy) on {rows} of {N} output rows of the {N}x{K} layer "
                       f"with all T={T} calibration tokens and {len(alphas)} alphas plus the "
                       f"M={list(gemm_m)} matmuls; statistic over the full X; time extrapolated "
                       f"linearly in rows to the whole layer",
-            "seconds_per_layer": sec, "sample_seconds": d["t_stats"] + d["t_rows"]}
+            "seconds_per_layer": sec, "sample_seconds": d["t_stats"] + d["t_rows"],
+            "single_thread": oracle_single_thread(layer, s, G)}
 
 
 def run_reference(args):
+    """The oracle as the reference arm. Each step times the statistic over the whole X and the
+    search, pack and matmuls of a bounded slice of output rows; ``ms_per_step`` is that measured
+    time, and ``value`` the layers/s of the whole layer extrapolated linearly in rows from it
+    (``extrapolated_ms_per_layer``), since one oracle layer takes minutes."""
     rank, _, world = dist_env()
     if rank != 0:
         return 0
@@ -401,31 +455,33 @@ def run_reference(args):
     G = wl.group_size
     total_steps = args.steps + args.warmup
     budget = max(1.0, min(8.0, 150.0 / max(total_steps, 1)))
-    rows, m = choose_rows(layer, alphas, wl.gemm_m, G, budget)
-    from oracle import awq_ref as ref
-    t0 = time.perf_counter()
-    ref.calib_stats(layer["X"])                     # the statistic is row-independent: once
-    t_stats = time.perf_counter() - t0
-    per = []
+    rows, _ = choose_rows(layer, alphas, wl.gemm_m, G, budget)
+    step_s, layer_s = [], []
     for i in range(total_steps):
-        sec, _ = oracle_layer_seconds(layer, alphas, wl.gemm_m, G, rows, m_cache=m)
+        t0 = time.perf_counter()
+        sec, _ = oracle_layer_seconds(layer, alphas, wl.gemm_m, G, rows)
         if i >= args.warmup:
-            per.append(sec + t_stats)
-    mean_s = sum(per) / len(per)
-    value = 1.0 / mean_s
-    sample = (f"each step: oracle (fp64 numpy) on {rows} of {spec.n} output rows of the "
-              f"{spec.n}x{spec.k} layer, all T={spec.t} tokens, {len(alphas)} alphas, pack and "
-              f"the M={list(wl.gemm_m)} matmuls, extrapolated linearly in rows; the statistic "
-              f"over the full X is timed once ({t_stats:.2f} s) and added to every step")
+            step_s.append(time.perf_counter() - t0)
+            layer_s.append(sec)
+    mean_step = sum(step_s) / len(step_s)
+    mean_layer = sum(layer_s) / len(layer_s)
+    value = 1.0 / mean_layer
+    sample = (f"each step: oracle (fp64 numpy) statistic over the full X, then the search of "
+              f"{len(alphas)} alphas, the pack and the M={list(wl.gemm_m)} matmuls on {rows} of "
+              f"{spec.n} output rows of the {spec.n}x{spec.k} layer with all T={spec.t} tokens; "
+              f"ms_per_step is the measured step time, value the whole layer extrapolated "
+              f"linearly in rows (extrapolated_ms_per_layer)")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": mean_s * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": mean_step * 1e3,
+        "extrapolated_ms_per_layer": mean_layer * 1e3, "rows_per_step": rows,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "N": spec.n, "K": spec.k, "T": spec.t,
                    "group_size": G, "n_alpha": len(alphas), "gemm_m": list(wl.gemm_m)},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -709,21 +765,21 @@ def run_ours(args):
     return 0
 
 
-# kernel name -> (kernel description, bound, committed ncu summary, source file)
+# kernel name -> (kernel description, bound, committed ncu summary or None, source files)
 ROOFLINE_KERNELS = {
     "gram_search": ("search_kernel: one persistent cooperative launch, tcgen05 kind::f16 X^T X "
                     "triangle then D B^T over the triangle per alpha, next residual built in "
                     "extra warps", "tensor", "gram_search_llama7b_attn_4096.md",
                     ("gram_persistent.cuh", "gram_score.cuh", "quant.cuh")),
     "score_gram": ("tri_kernel<SCORE>: tcgen05 kind::f16 D B^T over the triangle, fp32 "
-                   "accumulate, d . (D B^T) epilogue", "tensor",
-                   "score_gram_llama7b_attn_4096.md", ("gram_score.cuh", "quant.cuh")),
-    "gram": ("tri_kernel<GRAM>: tcgen05 kind::f16 lower triangle of X^T X", "tensor",
-             "gram_llama7b_attn_4096.md", ("gram_score.cuh", "quant.cuh")),
+                   "accumulate, d . (D B^T) epilogue", "tensor", None,
+                   ("gram_score.cuh", "quant.cuh")),
+    "gram": ("tri_kernel<GRAM>: tcgen05 kind::f16 lower triangle of X^T X", "tensor", None,
+             ("gram_score.cuh", "quant.cuh")),
     "score": ("score_kernel: tcgen05 kind::f16 X D^T, fp32 accumulate, sum of squares", "tensor",
-              "score_kernel_llama7b_attn_4096.md", ("score_gemm.cuh",)),
-    "residual": ("residual_kernel: W - Q(W diag s) diag(s)^-1 as fp16", "hbm",
-                 "residual_kernel_llama7b_attn_4096.md", ("quant.cuh",)),
+              None, ("score_gemm.cuh",)),
+    "residual": ("residual_kernel: W - Q(W diag s) diag(s)^-1 as fp16", "hbm", None,
+                 ("quant.cuh",)),
 }
 
 

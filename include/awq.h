@@ -193,7 +193,9 @@ awq_status_t awq_quant_residual(const void* W_f16, int64_t N, int64_t K, const f
 /*
  * W4A16 dequant-fused matmul: Y [M, N] fp16 = X [M, K] fp16 @ (dequant(Q) diag(inv_s))^T,
  * fp32 accumulation. inv_s [K] fp32 or NULL (1/s already folded into the previous layer).
- * M <= 8 runs a CUDA-core GEMV; larger M runs the tcgen05 tensor-core kernel. With inv_s,
+ * M <= 2 runs a CUDA-core GEMV (integer inner products on block fixed-point activations);
+ * 3 <= M <= 16 with G >= 64 the tcgen05 grouped kernel; every other M the tcgen05 dequant
+ * kernel. With inv_s,
  * X * inv_s must stay inside the fp16 range (as the folded activation would).
  */
 awq_status_t awq_w4a16_gemm(const void* X_f16, int64_t M, int64_t N, int64_t K,
@@ -235,11 +237,14 @@ uint64_t awq_set_wait_limit_ns(uint64_t limit_ns);
  * that loads the library holds until the process exits. Shapes whose smallest workspace (one
  * residual buffer, see awq_search_workspace_bytes) exceeds it return AWQ_ERR_WORKSPACE without
  * launching (the 4096 x 4096 layer with 20 alphas needs about 33 MiB); shapes that fit twice
- * over use the overlapped schedule. The call allocates nothing.
+ * over use the overlapped schedule. Arguments are checked exactly as awq_search_scale checks
+ * them (same error codes, in the same order) before the size of the shape is compared with the
+ * array. The call allocates no device memory.
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, which
- * may load this library's device code on that device); make that first call before any stream
- * capture. Every call shares the one array and leaves its contents behind; the search writes
+ * may load this library's device code on that device); like the first call of any search entry
+ * point on a device, it also creates the library's second stream and the events that order it
+ * (see awq_search_scale). Make that first call before any stream capture. Every call shares the one array and leaves its contents behind; the search writes
  * everything it later reads and clears its own max|W| word, so no clearing is needed between
  * calls. Calls whose work overlaps on the GPU (for example on two streams at once) race on the
  * array: serialise them.

@@ -158,7 +158,18 @@ def awq_search_scale_static(W, N, K, X, T, mean_abs, alphas, n_alpha, group_size
         _ptr(inv_s_out), _stream(stream)))
 
 
-SEARCH_STATIC_SCRATCH_BYTES = 40 * 1024 * 1024
+def _header_scratch_bytes() -> int:
+    """AWQ_SEARCH_STATIC_SCRATCH_BYTES as the C header defines it (``(a u * b u * ...)``)."""
+    m = re.search(r"#define\s+AWQ_SEARCH_STATIC_SCRATCH_BYTES\s+\(([^)]*)\)", open(HEADER).read())
+    if m is None:
+        raise RuntimeError("AWQ_SEARCH_STATIC_SCRATCH_BYTES is not defined in include/awq.h")
+    n = 1
+    for f in m.group(1).split("*"):
+        n *= int(f.strip().rstrip("uUlL"))
+    return n
+
+
+SEARCH_STATIC_SCRATCH_BYTES = _header_scratch_bytes()
 
 
 def awq_quantize_pack(W, N, K, s, group_size, symmetric, qweight, scales, zeros, stream=None,

@@ -861,6 +861,31 @@ awq_status_t awq_quant_residual(const void* W_f16, int64_t N, int64_t K, const f
 }  // extern "C"
 
 namespace awq {
+// Every argument check of the search except those on the workspace, in the order
+// awq_search_scale makes them: configuration, NULL pointers and counts, sizes, alignment, and
+// the shape a forced Gram score mode needs. Shared with the static-scratch search, so both
+// report the same error for the same bad argument.
+awq_status_t search_check_args(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
+                               int64_t T, const float* mean_abs, const float* alphas,
+                               int32_t n_alpha, awq_qcfg_t cfg, const float* err_out,
+                               const int32_t* best_idx, const float* s_out,
+                               const float* inv_s_out) {
+  AWQ_TRY(check_cfg(cfg));
+  if (!W_f16 || !X_f16 || !alphas || !err_out || !best_idx || T < 1) return AWQ_ERR_INVALID_ARG;
+  if (n_alpha < 1 || n_alpha > 64) return AWQ_ERR_INVALID_ARG;
+  AWQ_TRY(check_nk(N, K, cfg));
+  if (T * K > kMaxElems) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(W_f16) || !aligned16(X_f16) || (mean_abs && !aligned16(mean_abs)) ||
+      !aligned4(err_out) || !aligned4(best_idx) || (s_out && !aligned16(s_out)) ||
+      (inv_s_out && !aligned16(inv_s_out)))
+    return AWQ_ERR_MISALIGNED;
+  const int score_mode = g_score_mode.load();
+  if ((score_mode == AWQ_SCORE_GRAM || score_mode == AWQ_SCORE_GRAM_LAUNCHES) &&
+      !gram_shape_ok(K, T))
+    return AWQ_ERR_UNSUPPORTED_SHAPE;
+  return AWQ_OK;
+}
+
 // Smallest workspace awq_search_scale accepts (one residual buffer: candidates in order).
 size_t search_workspace_min_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
                                   awq_qcfg_t cfg) {
@@ -904,20 +929,11 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
                               int32_t n_alpha, awq_qcfg_t cfg, void* workspace,
                               size_t ws_bytes, float* err_out, int32_t* best_idx,
                               float* s_out, float* inv_s_out, awq_stream_t stream) {
-  AWQ_TRY(check_cfg(cfg));
-  if (!W_f16 || !X_f16 || !alphas || !err_out || !best_idx || T < 1) return AWQ_ERR_INVALID_ARG;
-  if (n_alpha < 1 || n_alpha > 64) return AWQ_ERR_INVALID_ARG;
-  AWQ_TRY(check_nk(N, K, cfg));
-  if (T * K > kMaxElems) return AWQ_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(W_f16) || !aligned16(X_f16) || (mean_abs && !aligned16(mean_abs)) ||
-      !aligned4(err_out) || !aligned4(best_idx) || (s_out && !aligned16(s_out)) ||
-      (inv_s_out && !aligned16(inv_s_out)) || !aligned16(workspace))
-    return AWQ_ERR_MISALIGNED;
+  AWQ_TRY(search_check_args(W_f16, N, K, X_f16, T, mean_abs, alphas, n_alpha, cfg, err_out,
+                            best_idx, s_out, inv_s_out));
+  if (!aligned16(workspace)) return AWQ_ERR_MISALIGNED;
   const SearchLayout L = search_layout(N, K, T, n_alpha);
   const int score_mode = g_score_mode.load();
-  if ((score_mode == AWQ_SCORE_GRAM || score_mode == AWQ_SCORE_GRAM_LAUNCHES) &&
-      !gram_shape_ok(K, T))
-    return AWQ_ERR_UNSUPPORTED_SHAPE;
   if (!workspace || ws_bytes < L.min_total) return AWQ_ERR_WORKSPACE;
   DeviceInfo* d = nullptr;
   AWQ_TRY(device_info(&d));

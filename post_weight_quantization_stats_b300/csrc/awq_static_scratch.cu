@@ -18,6 +18,11 @@
 namespace awq {
 size_t search_workspace_min_bytes(int64_t N, int64_t K, int64_t T, int32_t n_alpha,
                                   awq_qcfg_t cfg);
+awq_status_t search_check_args(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
+                               int64_t T, const float* mean_abs, const float* alphas,
+                               int32_t n_alpha, awq_qcfg_t cfg, const float* err_out,
+                               const int32_t* best_idx, const float* s_out,
+                               const float* inv_s_out);
 }
 
 namespace {
@@ -58,12 +63,16 @@ extern "C" awq_status_t awq_search_scale_static(const void* W_f16, int64_t N, in
                                                 int32_t n_alpha, awq_qcfg_t cfg, float* err_out,
                                                 int32_t* best_idx, float* s_out,
                                                 float* inv_s_out, awq_stream_t stream) {
+  // the workspace search's own argument checks first, so a bad pointer, size or alignment
+  // gets the same error here as there; only valid inputs can be refused for their size
+  const awq_status_t valid = awq::search_check_args(W_f16, N, K, X_f16, T, mean_abs, alphas,
+                                                    n_alpha, cfg, err_out, best_idx, s_out,
+                                                    inv_s_out);
+  if (valid != AWQ_OK) return valid;
   // the smallest workspace the search runs with (one residual buffer, candidates in order)
   const size_t need = awq::search_workspace_min_bytes(N, K, T, n_alpha, cfg);
-  if (need == 0)  // invalid shape or configuration: report the search's own validation error
-    return awq_search_scale(W_f16, N, K, X_f16, T, mean_abs, alphas, n_alpha, cfg, nullptr, 0,
-                            err_out, best_idx, s_out, inv_s_out, stream);
-  if (need > static_cast<size_t>(AWQ_SEARCH_STATIC_SCRATCH_BYTES)) return AWQ_ERR_WORKSPACE;
+  if (need == 0 || need > static_cast<size_t>(AWQ_SEARCH_STATIC_SCRATCH_BYTES))
+    return AWQ_ERR_WORKSPACE;
   void* scratch = nullptr;
   const awq_status_t st = scratch_for_current_device(&scratch);
   if (st != AWQ_OK) return st;

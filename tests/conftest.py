@@ -19,6 +19,12 @@ def pytest_collection_modifyitems(config, items):
     pass
 
 
+def pytest_terminal_summary(terminalreporter):
+    from tests import search_report
+    for line in search_report.summary_lines():
+        terminalreporter.write_line(line)
+
+
 @pytest.fixture(scope="session")
 def oracle():
     from oracle import awq_ref

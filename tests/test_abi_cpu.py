@@ -159,3 +159,40 @@ def test_launch_counter_starts_without_launches(L):
     assert awq.awq_launch_count() >= 0
     old = awq.awq_set_wait_limit_ns(123)
     assert awq.awq_set_wait_limit_ns(old) == 123
+
+
+def test_static_search_checks_arguments_before_its_size(L):
+    """awq_search_scale_static makes awq_search_scale's argument checks first: for a layer too
+    large for its static array, a NULL pointer, a misaligned pointer or T K beyond 2^31 gets the
+    same error as from the workspace entry point; only valid inputs are refused for their size
+    (AWQ_ERR_WORKSPACE). All of it before any CUDA call."""
+    cfg = awq.QCfg(128, 0)
+    A = 1 << 20
+    S = awq.STATUS_CODE
+    alphas = (ctypes.c_float * 2)(0.0, 0.5)
+    ap = ctypes.cast(alphas, ctypes.c_void_p)
+    N = K = 8192
+    T = 64
+    assert awq.awq_search_workspace_bytes(N, K, T, 2) > awq.SEARCH_STATIC_SCRATCH_BYTES
+
+    def static(W=A, X=A, T=T, alphas=ap, n_alpha=2, err=A, best=A, s=None, inv=None, cfg=cfg):
+        return L.awq_search_scale_static(W, N, K, X, T, None, alphas, n_alpha, cfg, err, best, s,
+                                         inv, None)
+
+    def workspace(W=A, X=A, T=T, alphas=ap, n_alpha=2, err=A, best=A, s=None, inv=None, cfg=cfg):
+        return L.awq_search_scale(W, N, K, X, T, None, alphas, n_alpha, cfg, A, 1 << 40, err,
+                                  best, s, inv, None)
+
+    for kw, want in (({"W": None}, "AWQ_ERR_INVALID_ARG"), ({"best": None}, "AWQ_ERR_INVALID_ARG"),
+                     ({"alphas": None}, "AWQ_ERR_INVALID_ARG"), ({"n_alpha": 0}, "AWQ_ERR_INVALID_ARG"),
+                     ({"cfg": awq.QCfg(96, 0)}, "AWQ_ERR_INVALID_ARG"),
+                     ({"X": A + 2}, "AWQ_ERR_MISALIGNED"), ({"s": A + 4}, "AWQ_ERR_MISALIGNED"),
+                     ({"T": 1 << 19}, "AWQ_ERR_UNSUPPORTED_SHAPE")):
+        assert static(**kw) == S[want], kw
+        assert workspace(**kw) == S[want], kw
+    assert static() == S["AWQ_ERR_WORKSPACE"]
+    # a shape the array holds passes every host check and stops only at the device lookup
+    import torch
+    if not torch.cuda.is_available():
+        assert L.awq_search_scale_static(A, 16, 256, A, 8, None, ap, 2, cfg, A, A, None, None,
+                                         None) == S["AWQ_ERR_NO_DEVICE"]

@@ -5,7 +5,8 @@ vector, so both sides decide each code in fp32 from the same operands); the stat
 1e-5 relative (fp32 accumulation vs fp64); the alpha errors within 1e-3 relative (for layers
 with fewer than 4096 outputs T*N, within the larger of that and the bound the fp16 residual and
 fp32 accumulation imply, since a handful of outputs cannot average the rounding out) and the
-chosen alpha index exact (unless the oracle's own errors are a near-tie within those bounds);
+chosen alpha index exact (unless the oracle's own errors are a near-tie: within 1e-4 relative,
+or, for those tiny layers, within the analytic bounds; each accepted near-tie is reported);
 W4A16 outputs within 2e-2 of max|reference| against the oracle's fp64 dequant-matmul.
 """
 
@@ -20,6 +21,7 @@ torch = pytest.importorskip("torch")
 
 from oracle import awq_ref as ref  # noqa: E402
 from post_weight_quantization_stats_b300 import awq, build, synth  # noqa: E402
+from tests import search_report  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -199,13 +201,36 @@ def score_mode(mode):
         awq.awq_set_score_mode("auto")
 
 
-def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False, gram=False, bits=4):
-    W, X = dev(W16), dev(X16)
-    m = awq.calib_stats(X) if use_m else None
-    err, best, s, inv_s = awq.search_scale(W, X, alphas, G, sym, mean_abs=m, bits=bits)
-    awq.awq_stream_status()
-    m_gpu = host(awq.calib_stats(X))
-    r = ref.search_scale(W16, X16, alphas, G, sym, m=m_gpu, bits=bits)
+def _check_alpha_index(b, r, bound, label):
+    """The chosen alpha index against the oracle's argmin (first minimiser of its fp64 errors).
+
+    It must be the same index. The one exception is a near-tie of the oracle's own errors:
+    E_oracle(b) <= E_oracle(best) (1 + 1e-4). For layers with fewer than 4096 outputs, where the
+    error tolerance is the analytic bound of the GPU's arithmetic (``bound``, zero otherwise),
+    a pick whose oracle gap lies within the two candidates' bounds is a near-tie too: the GPU's
+    errors may then order them either way. Every comparison is recorded and every accepted
+    near-tie is listed in the run's summary."""
+    best = int(r["best"])
+    e = r["err"]
+    srt = np.sort(e)
+    runner = (srt[1] - srt[0]) / srt[0] if len(e) > 1 and srt[0] > 0 else np.inf
+    search_report.compared(label, b, best, runner)
+    if b == best:
+        return
+    allowed = 1e-4 * e[best]
+    if np.ndim(bound):
+        allowed = max(allowed, bound[b] + bound[best])
+    gap = e[b] - e[best]
+    assert gap <= allowed, (label, b, best, e)
+    search_report.accepted(label, b, best, gap / e[best] if e[best] > 0 else 0.0,
+                           allowed / e[best] if e[best] > 0 else 0.0)
+
+
+def _compare_search(got, r, X16, W16, G, sym, bits, gram, label):
+    """GPU search results ``got`` = (err, best, s, inv_s) against the oracle's ``r``: every error
+    within 1e-3 relative (tiny layers: the analytic bound, n18), the alpha index by
+    _check_alpha_index, s and 1/s of the chosen alpha within 1e-6."""
+    err, best, s, inv_s = got
     e = host(err).astype(np.float64)
     small = X16.shape[0] * W16.shape[0] < 4096
     bound = 0.0
@@ -214,14 +239,27 @@ def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False, gram=False, b
         if gram:
             bound = bound + _gram_bound(X16, W16, r["s_grid"], G, sym, bits)
     tol = np.maximum(1e-3 * r["err"], bound)
-    assert np.all(np.abs(e - r["err"]) <= tol), (e, r["err"], tol)
+    assert np.all(np.abs(e - r["err"]) <= tol), (label, e, r["err"], tol)
     b = int(host(best)[0])
-    if b != r["best"]:   # only a near-tie of the oracle's own errors may pick another alpha
-        slack = max(1e-4 * r["err"][r["best"]], tol[b] + tol[r["best"]])
-        assert r["err"][b] <= r["err"][r["best"]] + slack, (b, r["best"], r["err"])
+    _check_alpha_index(b, r, bound, label)
     np.testing.assert_allclose(host(s), r["s_grid"][b], rtol=1e-6, atol=0)
     np.testing.assert_allclose(host(inv_s), (np.float32(1) / r["s_grid"][b]).astype(np.float32),
                                rtol=1e-6, atol=0)
+    return e, b
+
+
+def _check_search(W16, X16, alphas, G=128, sym=False, use_m=False, gram=False, bits=4,
+                  label=None):
+    W, X = dev(W16), dev(X16)
+    m = awq.calib_stats(X) if use_m else None
+    got = awq.search_scale(W, X, alphas, G, sym, mean_abs=m, bits=bits)
+    awq.awq_stream_status()
+    m_gpu = host(awq.calib_stats(X))
+    r = ref.search_scale(W16, X16, alphas, G, sym, m=m_gpu, bits=bits)
+    if label is None:
+        label = f"{W16.shape[0]}x{W16.shape[1]} T={X16.shape[0]} G={G} sym={int(sym)} " \
+                f"bits={bits}{' gram' if gram else ''}"
+    e, b = _compare_search(got, r, X16, W16, G, sym, bits, gram, label)
     return e, b, r
 
 
@@ -445,10 +483,88 @@ def test_search_gram_large_activation_range():
 
 @pytest.mark.slow
 def test_search_full_size_llama7b_attn():
-    """K = N = 4096, T = 8192 (the benchmark's layer), in the benchmark's launch configuration:
-    the oracle's fp64 error at alpha_0 and at the chosen alpha, the codes of the chosen alpha,
-    and the argmin property over all 20."""
+    """K = N = 4096, T = 8192 (the benchmark's layer), in the benchmark's launch configuration
+    (AUTO: the persistent Gram launch): all 20 errors within 1e-3 of the oracle's fp64 search of
+    the whole layer, the alpha index by the near-tie rule, the codes of the chosen alpha
+    bit-exact."""
     d = synth.make_layer("llama7b-attn-4096")
+    W16, X16 = d["W"], d["X"]
+    alphas = synth.alpha_grid(20)
+    W, X = dev(W16), dev(X16)
+    got = awq.search_scale(W, X, alphas)
+    awq.awq_stream_status()
+    m_gpu = host(awq.calib_stats(X))
+    r = ref.search_scale(W16, X16, alphas, m=m_gpu)
+    e, b = _compare_search(got, r, X16, W16, 128, False, 4, True, "llama7b-attn-4096 (full)")
+    assert np.all(np.isfinite(e)) and e[b] <= e[0]
+    q, sc, z = awq.quantize_pack(W, got[2])
+    want = ref.quantize_pack(W16, host(got[2]))
+    assert np.array_equal(host(q).view(np.uint32), want["qweight"])
+    assert np.array_equal(host(sc), want["scales"])
+    assert np.array_equal(host(z), want["zeros"])
+
+
+# the Llama-7B MLP (gate/up 4096 -> 11008, down 11008 -> 4096, T = 8192) and Llama-70B MLP
+# (8192 -> 28672 and back, T = 4096) layers: (workload, layer index)
+WORKLOAD_LAYERS = [("llama7b-mlp", 0), ("llama7b-mlp", 2), ("llama70b-mlp", 0),
+                   ("llama70b-mlp", 1)]
+_layer_cache = {}
+
+
+def _workload_layer(wl, i):
+    key = (wl, i)
+    if key not in _layer_cache:
+        _layer_cache.clear()          # one full-size layer held at a time
+        _layer_cache[key] = synth.make_layer(wl, i)
+    return _layer_cache[key]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wl,i", WORKLOAD_LAYERS)
+def test_search_workload_row_slice(wl, i):
+    """The search at the real K and T of the MLP workloads on the first 512 output rows (the
+    oracle's fp64 search of the whole layer would take too long): the oracle searches the slice
+    once, and the GPU searches it under each score form (AUTO takes the direct one for 512
+    rows; GRAM forced), every error within 1e-3 and the alpha index by the near-tie rule."""
+    d = _workload_layer(wl, i)
+    W16 = np.ascontiguousarray(d["W"][:512])
+    X16 = d["X"]
+    alphas = synth.alpha_grid(20)
+    W, X = dev(W16), dev(X16)
+    m = awq.calib_stats(X)
+    r = ref.search_scale(W16, X16, alphas, m=host(m))
+    results = {}
+    for mode in ("auto", "gram", "direct"):
+        with score_mode(mode):
+            got = awq.search_scale(W, X, alphas, mean_abs=m)
+            awq.awq_stream_status()
+        label = f"{wl}[{i}] {d['spec'].name} rows 0-511 K={W16.shape[1]} T={X16.shape[0]} {mode}"
+        results[mode] = _compare_search(got, r, X16, W16, 128, False, 4, mode == "gram", label)
+    assert np.array_equal(results["auto"][0], results["direct"][0])    # AUTO is DIRECT here
+
+
+def _oracle_error_rows(X16, W16, s, chunk=2048):
+    """The oracle's error of the codes of W diag(s) over the whole layer, its rows taken in
+    chunks (the mean over tokens and outputs is a sum over rows divided by T N)."""
+    X64 = X16.astype(np.float64)
+    total = 0.0
+    for n0 in range(0, W16.shape[0], chunk):
+        Wc = W16[n0:n0 + chunk]
+        qd = ref.quantize_pack(Wc, s)
+        w_hat = ref.dequantize(qd["qweight"], qd["scales"], qd["zeros"], 128, s=s)
+        total += float(np.sum((X64 @ (Wc.astype(np.float64) - w_hat).T) ** 2))
+    return total / (X16.shape[0] * W16.shape[0])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wl,i", WORKLOAD_LAYERS)
+def test_search_workload_full_size(wl, i):
+    """The whole layer in the launch configuration the benchmark times (AUTO: the Gram launch
+    for the 7B MLP layers, the direct one for the 70B layers). The oracle computes the errors
+    of alpha_0 (plain RTN) and of the chosen alpha and its grid neighbours over the whole layer:
+    each within 1e-3 of the GPU's, and the chosen alpha a minimum of the three by the near-tie
+    rule. The codes of the chosen alpha are bit-exact on 256 sampled rows."""
+    d = _workload_layer(wl, i)
     W16, X16 = d["W"], d["X"]
     alphas = synth.alpha_grid(20)
     W, X = dev(W16), dev(X16)
@@ -456,18 +572,22 @@ def test_search_full_size_llama7b_attn():
     awq.awq_stream_status()
     e = host(err).astype(np.float64)
     b = int(host(best)[0])
-    assert b == int(np.argmin(e)) and np.all(np.isfinite(e))
-    s_b = host(s)
+    assert np.all(np.isfinite(e)) and b == int(np.argmin(e)) and e[b] <= e[0]
+    s_grid = ref.fl32(ref.scale_grid(host(awq.calib_stats(X)), alphas))
+    np.testing.assert_allclose(host(s), s_grid[b], rtol=1e-6, atol=0)
+    idx = sorted({0, b, max(b - 1, 0), min(b + 1, len(alphas) - 1)})
+    e_or = {j: _oracle_error_rows(X16, W16, s_grid[j]) for j in idx}
+    for j in idx:
+        np.testing.assert_allclose(e[j], e_or[j], rtol=1e-3, err_msg=f"alpha index {j}")
+    r = {"err": np.array([e_or[j] for j in idx]), "best": int(np.argmin([e_or[j] for j in idx]))}
+    _check_alpha_index(idx.index(b), r, 0.0, f"{wl}[{i}] {d['spec'].name} (full, local argmin)")
+    rng = np.random.Generator(np.random.PCG64(i))
+    rows = np.sort(rng.choice(W16.shape[0], 256, replace=False))
     q, sc, z = awq.quantize_pack(W, s)
-    want = ref.quantize_pack(W16, s_b)
-    assert np.array_equal(host(q).view(np.uint32), want["qweight"])
-    e_b = ref.error_of_codes(X16, W16, want["qweight"], want["scales"], want["zeros"], s_b)
-    np.testing.assert_allclose(e[b], e_b, rtol=1e-3)
-    rtn = ref.quantize_pack(W16, None)
-    e_0 = ref.error_of_codes(X16, W16, rtn["qweight"], rtn["scales"], rtn["zeros"],
-                             np.ones(W16.shape[1], np.float32))
-    np.testing.assert_allclose(e[0], e_0, rtol=1e-3)
-    assert e[b] <= e[0]
+    want = ref.quantize_pack(W16[rows], host(s))
+    assert np.array_equal(host(q)[rows].view(np.uint32), want["qweight"])
+    assert np.array_equal(host(sc)[:, rows], want["scales"])
+    assert np.array_equal(host(z)[:, rows], want["zeros"])
 
 
 # ----------------------------------------------------------------------------- W4A16 matmul

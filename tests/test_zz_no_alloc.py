@@ -4,8 +4,10 @@ The static variant serves callers that cannot allocate device memory where they 
 (a fixed memory budget set at start-up, a plug-in given a device but no allocator, a process
 whose allocations belong to another runtime): its scratch is a static array inside the library.
 It must give the same results as the workspace entry point, call after call, and must not
-allocate. This file sorts last so that a run stopping at the first failure has already run every
-other test.
+allocate. Where both entry points take the same schedule (every case here: the workspace
+search gets the workspace it asks for, and the static array holds that schedule's workspace),
+the results are the same bits. This file sorts last so that a run stopping at the first
+failure has already run every other test.
 """
 
 import numpy as np
@@ -33,40 +35,54 @@ def _outputs(n_alpha, K):
             torch.full((K,), float("nan"), dtype=torch.float32, device="cuda"))
 
 
-@pytest.mark.parametrize("which", ["tiny-512", "ragged"])
+# tiny-512 and the ragged layer take the direct scoring with two residual buffers; the third
+# has more calibration tokens than twice its input channels, so both entry points score through
+# H = X^T X in the persistent launch, whose cross-CTA counters, X^T and H's triangle then live
+# in the static array
+CASES = {
+    "tiny-512": lambda: synth.make_layer("tiny-512"),
+    "ragged": lambda: synth.random_layer(11, 1000, 2048, 300, n_out=10),
+    "gram": lambda: synth.random_layer(12, 2048, 1024, 4096, n_out=10),
+}
+
+
+@pytest.mark.parametrize("which", sorted(CASES))
 def test_static_search_matches_workspace_search_on_two_calls(which):
-    d = synth.make_layer("tiny-512") if which == "tiny-512" else \
-        synth.random_layer(11, 1000, 2048, 300, n_out=10)
+    d = CASES[which]()
     W = torch.from_numpy(d["W"]).cuda()
     X = torch.from_numpy(d["X"]).cuda()
     N, K = W.shape
     T = X.shape[0]
     alphas = synth.alpha_grid(20)
-    ref_err, ref_best, ref_s, ref_inv = awq.search_scale(W, X, alphas)
+    assert awq.awq_search_workspace_bytes(N, K, T, 20) <= awq.SEARCH_STATIC_SCRATCH_BYTES
+    want = awq.search_scale(W, X, alphas)
     awq.awq_stream_status()
     for call in range(2):
-        err, best, s, inv = _outputs(len(alphas), K)
+        got = _outputs(len(alphas), K)
         torch.cuda.synchronize()
         free_before = torch.cuda.mem_get_info()[0]
-        awq.awq_search_scale_static(W, N, K, X, T, None, alphas, len(alphas), 128, False, err,
-                                    best, s, inv)
+        awq.awq_search_scale_static(W, N, K, X, T, None, alphas, len(alphas), 128, False, *got)
         awq.awq_stream_status()
         if call == 1:   # the first call may load the library's device code; later ones allocate nothing
             assert torch.cuda.mem_get_info()[0] == free_before
-        np.testing.assert_allclose(err.cpu().numpy(), ref_err.cpu().numpy(), rtol=1e-3, atol=0)
-        assert int(best.item()) == int(ref_best.item())
-        np.testing.assert_allclose(s.cpu().numpy(), ref_s.cpu().numpy(), rtol=1e-6, atol=0)
-        np.testing.assert_allclose(inv.cpu().numpy(), ref_inv.cpu().numpy(), rtol=1e-6, atol=0)
+        for name, u, v in zip(("err", "best", "s", "inv_s"), want, got):
+            assert torch.equal(u, v), (which, call, name)
+        assert np.all(np.isfinite(got[0].cpu().numpy()))
 
 
 def test_static_search_rejects_shapes_beyond_its_scratch():
-    W = torch.zeros((16, 256), dtype=torch.float16, device="cuda")
-    X = torch.zeros((16, 256), dtype=torch.float16, device="cuda")
-    err, best, s, inv = _outputs(20, 256)
-    need = awq.awq_search_workspace_bytes(8192, 8192, 4096, 20)
+    """A valid 8192 x 8192 layer (real buffers of that size): one residual buffer alone is
+    128 MiB, beyond the static array, so the call is refused before anything is launched."""
+    N = K = 8192
+    T = 64
+    W = torch.zeros((N, K), dtype=torch.float16, device="cuda")
+    X = torch.zeros((T, K), dtype=torch.float16, device="cuda")
+    err, best, s, inv = _outputs(20, K)
+    need = awq.awq_search_workspace_bytes(N, K, T, 20)
     assert need > awq.SEARCH_STATIC_SCRATCH_BYTES
     with pytest.raises(awq.AwqError) as ei:
-        awq.awq_search_scale_static(W, 8192, 8192, X, 4096, None, synth.alpha_grid(20), 20, 128,
-                                    False, err, best, s, inv)
+        awq.awq_search_scale_static(W, N, K, X, T, None, synth.alpha_grid(20), 20, 128, False,
+                                    err, best, s, inv)
     assert ei.value.name == "AWQ_ERR_WORKSPACE"
-    assert torch.isnan(err).all()          # nothing was launched
+    torch.cuda.synchronize()
+    assert torch.isnan(err).all() and int(best.item()) == -1   # nothing was launched
