@@ -14,9 +14,10 @@ Recipe (what each draw stands in for):
   activation property") puts the salient fraction at roughly 0.1%-1% of channels; the
   Benefits page puts the calibration set at 128-512 samples. Where the outlier recipe asks for
   heavy tails, the outlier channels are Student-t (nu=3) draws.
-* The MLP down-projection's calibration input is the gated activation of the generated
-  ``X``: ``fp16(silu(X W_gate^T) * (X W_up^T))`` with fp32 accumulation on the host. That is
-  the model's forward pass, not part of AWQ.
+* The MLP down-projection's calibration input in the Llama-7B MLP and the 7B-like stack is the
+  gated activation of the generated ``X``: ``fp16(silu(X W_gate^T) * (X W_up^T))`` with fp32
+  accumulation on the host. That is the model's forward pass, not part of AWQ. The Llama-70B
+  layers both take plain draws with 1% outlier channels (no gating), as that workload states.
 
 No public dataset or trained checkpoint is used or needed: these draws stand in for the
 "calibration data" and model weights the pages talk about.
@@ -44,6 +45,7 @@ class LayerSpec:
     outlier_mult: float  # multiplier applied to outlier channels
     outlier_student_t: bool = False  # outlier channels drawn from Student-t (nu=3)
     outlier_count: int | None = None  # explicit outlier channel count (overrides frac)
+    gated: bool = False  # MLP down-projection: input = fp16(silu(gate) * up) of the block's X
 
 
 @dataclasses.dataclass(frozen=True)
@@ -77,7 +79,7 @@ WORKLOADS = {
         3, "llama7b-mlp",
         (LayerSpec("gate_proj", 11008, 4096, 8192, 0.02, 0.005, 10.0, True, 20),
          LayerSpec("up_proj", 11008, 4096, 8192, 0.02, 0.005, 10.0, True, 20),
-         LayerSpec("down_proj", 4096, 11008, 8192, 0.02, 0.0, 1.0, False, 0)),
+         LayerSpec("down_proj", 4096, 11008, 8192, 0.02, 0.0, 1.0, False, 0, gated=True)),
         (1, 2, 4, 8, 16, 32),
         description="Llama-7B-shaped MLP gate/up 4096->11008 and down 11008->4096, T=8192; "
                     "down-proj input = fp16(silu(gate) * up) of the generated X",
@@ -93,7 +95,7 @@ WORKLOADS = {
     "llama7b-stack": Workload(
         5, "llama7b-stack",
         tuple(
-            LayerSpec(f"l{i}.{p}", n, k, 2048, 0.02, 0.01, 20.0, False)
+            LayerSpec(f"l{i}.{p}", n, k, 2048, 0.02, 0.01, 20.0, False, gated=(p == "down"))
             for i in range(32)
             for p, n, k in (("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096),
                             ("o", 4096, 4096), ("gate", 11008, 4096), ("up", 11008, 4096),
@@ -174,7 +176,7 @@ def make_layer(workload, layer_index: int = 0, t: int | None = None,
     spec = wl.layers[layer_index % len(wl.layers)]
     rng = rng_for(wl.wid, layer_index)
     w = draw_weight(rng, spec.n, spec.k, spec.sigma)
-    if spec.name.endswith("down_proj") or spec.name.endswith(".down"):
+    if spec.gated:
         gate_i, up_i = _gate_up_indices(wl, layer_index)
         g = make_layer(wl, gate_i, t=t)
         up_spec = wl.layers[up_i % len(wl.layers)]
