@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hbm-sweep", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the search at the 7B-MLP, 70B-MLP and 224-linear stack workloads")
     ap.add_argument("--case", default=None,
                     help="run one kernel family on a small case and exit (for profiler "
                          "captures): 'search' (statistic, alpha search and pack of the "
@@ -568,11 +570,13 @@ def w4a16_graph_time(awq, torch, N, K, G, M, sets, inv, reps_outer=3):
 
 def w4a16_sweep(awq, torch, shapes, ms, G, peaks):
     """W4A16 throughput per (shape, M): HBM GB/s of the algorithmic bytes (packed weights +
-    metadata + activations + outputs + inv_s) and TFLOP/s, each against the measured peaks."""
+    metadata + activations + outputs + inv_s) and TFLOP/s, each against the measured peaks.
+    ``ms`` is one list of M for every shape, or a list of lists (one per shape)."""
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20)
     gen = torch.Generator(device="cuda").manual_seed(7)
     out = []
-    for N, K in shapes:
+    per_shape = ms if ms and isinstance(ms[0], (list, tuple)) else [ms] * len(shapes)
+    for (N, K), ms in zip(shapes, per_shape):
         packed = N * K // 2 + 3 * N * (K // G)
         copies = int(max(2, -(-2 * l2 // packed)))
         sets = [(torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32,
@@ -599,53 +603,380 @@ def w4a16_sweep(awq, torch, shapes, ms, G, peaks):
     return out
 
 
-def stack_decode(awq, torch, peaks, G=128, M=1):
-    """One decode step (M tokens) through all 224 linears of the synthetic 7B stack, captured in
-    one CUDA graph: weight bytes streamed per token against the HBM peak."""
+def stack_decode(awq, torch, peaks, G=128, ms=(1,), reps=5):
+    """Decode steps (M tokens) through all 224 linears of the synthetic 7B stack, each captured
+    in one CUDA graph: weight bytes streamed per step against the HBM peak, one entry per M.
+    The packed weights are drawn once (3.4 GB at G = 128, more than L2 many times over)."""
     wl = synth.WORKLOADS["llama7b-stack"]
     gen = torch.Generator(device="cuda").manual_seed(11)
-    layers = []
-    total = 0
+    weights = []
     for spec in wl.layers:
         N, K = spec.n, spec.k
-        layers.append((N, K,
-                       torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32,
-                                     device="cuda", generator=gen),
-                       (torch.rand((K // G, N), device="cuda", generator=gen) * 0.01 + 1e-3).half(),
-                       torch.randint(0, 16, (K // G, N), dtype=torch.uint8, device="cuda",
-                                     generator=gen),
-                       torch.randn((M, K), device="cuda", generator=gen).half(),
-                       torch.empty((M, N), dtype=torch.float16, device="cuda"),
-                       torch.rand(K, device="cuda", generator=gen) + 0.5))
-        total += N * K // 2 + 3 * N * (K // G) + 2 * M * K + 2 * M * N + 4 * K
-    for N, K, q, sc, z, X, Y, inv in layers[:7]:
-        awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y)
-    awq.awq_stream_status()
-    stream = torch.cuda.Stream()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            for N, K, q, sc, z, X, Y, inv in layers:
-                awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y, stream)
-    graph.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 5
-    e0.record()
-    for _ in range(reps):
+        weights.append((N, K,
+                        torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32,
+                                      device="cuda", generator=gen),
+                        (torch.rand((K // G, N), device="cuda", generator=gen) * 0.01 + 1e-3).half(),
+                        torch.randint(0, 16, (K // G, N), dtype=torch.uint8, device="cuda",
+                                      generator=gen),
+                        torch.rand(K, device="cuda", generator=gen) + 0.5))
+    out = []
+    for M in ms:
+        layers = []
+        total = 0
+        for N, K, q, sc, z, inv in weights:
+            layers.append((N, K, q, sc, z, torch.randn((M, K), device="cuda", generator=gen).half(),
+                           torch.empty((M, N), dtype=torch.float16, device="cuda"), inv))
+            total += N * K // 2 + 3 * N * (K // G) + 2 * M * K + 2 * M * N + 4 * K
+        for N, K, q, sc, z, X, Y, inv in layers[:7]:
+            awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y)
+        awq.awq_stream_status()
+        stream = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for N, K, q, sc, z, X, Y, inv in layers:
+                    awq.awq_w4a16_gemm(X, M, N, K, q, sc, z, inv, G, False, Y, stream)
         graph.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    awq.awq_stream_status()
-    ms = e0.elapsed_time(e1) / reps
-    gbs = total / (ms * 1e-3) / 1e9
-    del layers
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        awq.awq_stream_status()
+        t_ms = e0.elapsed_time(e1) / reps
+        gbs = total / (t_ms * 1e-3) / 1e9
+        out.append({"linears": len(wl.layers), "M": M, "group_size": G,
+                    "ms_per_token_step": round(t_ms, 4),
+                    "tokens_per_s": round(M / (t_ms * 1e-3), 1), "bytes_per_step": total,
+                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                    "roofline_ms": round(total / (peaks["hbm_gbs"] * 1e9) * 1e3, 4)})
+        del graph, layers
+    del weights
     torch.cuda.empty_cache()
-    return {"linears": len(wl.layers), "M": M, "group_size": G, "ms_per_token_step": round(ms, 4),
-            "tokens_per_s": round(M / (ms * 1e-3), 1), "bytes_per_step": total,
-            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-            "roofline_ms": round(total / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
-            "timing": "one CUDA graph of all linears, weights streamed from HBM"}
+    return out
+
+
+# ------------------------------------------------------------------------------ larger workloads
+#
+# The search at the other workloads' shapes (Llama-7B MLP, Llama-70B MLP, the 224-linear 7B-like
+# stack) and the W4A16 sweeps at their batch sizes. Inputs are drawn on the GPU by the same recipe
+# as synth.py (normal weights of the workload's sigma, normal activations with its outlier
+# channels, the gated down-projection input where the workload has one), seeded, so that
+# full-size layers need no host generation; the oracle comparisons at these shapes are in the
+# GPU tests, on synth.py's host draws.
+
+def gpu_layer(torch, spec, seed, gate=None):
+    """W [n, k] and X [t, k] fp16 on the device for one LayerSpec. ``gate`` = (X, W_gate, W_up)
+    of the block gives the gated down-projection input fp16(silu(X W_gate^T) * (X W_up^T))."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    W = (torch.randn((spec.n, spec.k), device="cuda", generator=g) * spec.sigma).half()
+    if gate is not None:
+        Xg, Wg, Wu = gate
+        xf = Xg.float()
+        h = torch.nn.functional.silu(xf @ Wg.float().T) * (xf @ Wu.float().T)
+        return W, h.half()
+    X = torch.randn((spec.t, spec.k), device="cuda", generator=g)
+    n_out = synth._n_outliers(spec)
+    if n_out:
+        idx = torch.randperm(spec.k, device="cuda", generator=g)[:n_out]
+        if spec.outlier_student_t:
+            torch.manual_seed(seed)
+            st = torch.distributions.StudentT(torch.tensor(3.0, device="cuda"))
+            X[:, idx] = st.sample((spec.t, n_out)) * spec.outlier_mult
+        else:
+            X[:, idx] *= spec.outlier_mult
+    return W, X.half()
+
+
+class SearchBuffers:
+    """Outputs and workspace of the per-layer step (statistic, search, pack) for one shape."""
+
+    def __init__(self, awq, torch, N, K, T, n_alpha, G, sym):
+        f32 = dict(dtype=torch.float32, device="cuda")
+        self.m = torch.empty(K, **f32)
+        self.err = torch.empty(n_alpha, **f32)
+        self.best = torch.empty(1, dtype=torch.int32, device="cuda")
+        self.s = torch.empty(K, **f32)
+        self.inv = torch.empty(K, **f32)
+        self.ws_bytes = awq.awq_search_workspace_bytes(N, K, T, n_alpha, G, sym)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.q = torch.empty((N, K // 8), dtype=torch.int32, device="cuda")
+        self.sc = torch.empty((K // G, N), dtype=torch.float16, device="cuda")
+        self.z = torch.empty((K // G, N), dtype=torch.uint8, device="cuda")
+
+    def outputs(self):
+        return [self.err, self.best, self.s, self.q, self.sc, self.z]
+
+
+def enqueue_layer(awq, W, X, alphas, G, sym, b, stream=None):
+    """Statistic, search and pack of one layer through the C ABI."""
+    N, K = W.shape
+    T = X.shape[0]
+    awq.awq_calib_stats(X, T, K, K, b.m, stream)
+    awq.awq_search_scale(W, N, K, X, T, b.m, alphas, len(alphas), G, sym, b.ws, b.ws_bytes,
+                         b.err, b.best, b.s, b.inv, stream)
+    awq.awq_quantize_pack(W, N, K, b.s, G, sym, b.q, b.sc, b.z, stream)
+
+
+def search_flops(N, K, T, n_alpha, sched):
+    """Flops of the search's scoring per layer: the direct form's n 2 T N K (the forward pass
+    per grid point), and what the schedule that ran computes (Gram: H's triangle once and
+    N K (K + 3) per candidate)."""
+    direct = n_alpha * 2 * T * N * K
+    if sched == "gram":
+        return direct, T * K * (K + 1) + n_alpha * N * K * (K + 3)
+    return direct, direct
+
+
+def schedule_of(prof):
+    return "gram" if ("gram_search" in prof or "score_gram" in prof) else "direct"
+
+
+def search_workloads(awq, torch, peaks, reps=3):
+    """Statistic + search + pack of the Llama-7B MLP (T = 8192) and Llama-70B MLP (T = 4096)
+    layers at full size: ms per layer (mean of ``reps`` after one warm-up, L2 flushed between
+    repetitions), layers/s, the schedule AUTO took and the search's roofline: the direct form's
+    flops at the measured bf16 peak against the measured time, and the dominant scoring kernel's
+    achieved TFLOP/s."""
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    out = []
+    for wl_name in ("llama7b-mlp", "llama70b-mlp"):
+        wl = synth.WORKLOADS[wl_name]
+        alphas = synth.alpha_grid(wl.n_alpha)
+        G = wl.group_size
+        gate = None
+        for li, spec in enumerate(wl.layers):
+            if wl_name == "llama7b-mlp" and spec.name == "up_proj":
+                continue                      # same shape as gate_proj
+            if spec.gated:
+                W, X = gpu_layer(torch, spec, 1000 * wl.wid + li, gate=gate)
+            else:
+                W, X = gpu_layer(torch, spec, 1000 * wl.wid + li)
+            if wl_name == "llama7b-mlp" and spec.name == "gate_proj":
+                Wu, _ = gpu_layer(torch, wl.layers[1], 1000 * wl.wid + 1)
+                gate = (X, W, Wu)
+            N, K = W.shape
+            T = X.shape[0]
+            b = SearchBuffers(awq, torch, N, K, T, len(alphas), G, False)
+            enqueue_layer(awq, W, X, alphas, G, False, b)
+            awq.awq_stream_status()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            awq.awq_profile_begin()
+            for i in range(reps):
+                flush.zero_()
+                ev[i][0].record()
+                enqueue_layer(awq, W, X, alphas, G, False, b)
+                ev[i][1].record()
+            torch.cuda.synchronize()
+            prof = awq.awq_profile_end()
+            awq.awq_stream_status()
+            ms = sum(a.elapsed_time(c) for a, c in ev) / reps
+            sched = schedule_of(prof)
+            direct, run_flops = search_flops(N, K, T, len(alphas), sched)
+            key = "gram_search" if sched == "gram" else "score"
+            n_k, ms_k = prof.get(key, (0, 0.0))
+            kern_tflops = None
+            if n_k:
+                per = ms_k / n_k * 1e-3
+                kern_tflops = (run_flops if sched == "gram" else run_flops / len(alphas)) / per / 1e12
+            roof_s = direct / (peaks["bf16_tflops"] * 1e12)
+            out.append({
+                "workload": wl_name, "layer": spec.name, "N": N, "K": K, "T": T, "schedule": sched,
+                "ms": round(ms, 3), "layers_per_s": round(1e3 / ms, 2),
+                "direct_form_tflop": round(direct / 1e12, 3),
+                "roofline_ms": round(roof_s * 1e3, 3), "frac_of_roofline": round(roof_s * 1e3 / ms, 4),
+                "scoring_kernel": key, "scoring_kernel_tflops": round(kern_tflops, 1) if kern_tflops else None,
+                "scoring_kernel_frac": round(kern_tflops / peaks["bf16_tflops"], 4) if kern_tflops else None,
+                "kernels_ms": {k: round(v[1] / reps, 3) for k, v in prof.items()},
+                "timing": f"statistic + search + pack, mean of {reps} after a warm-up, L2 flushed"})
+            del b, W, X
+            torch.cuda.empty_cache()
+        gate = None
+    return out
+
+
+def stack_layers(torch):
+    """The 224 linears of the synthetic 7B-like stack on the device (W and its calibration X;
+    the down-projections take the gated input of their block's gate and up projections)."""
+    wl = synth.WORKLOADS["llama7b-stack"]
+    layers = []
+    block = {}
+    for li, spec in enumerate(wl.layers):
+        if spec.gated:
+            W, X = gpu_layer(torch, spec, 1000 * wl.wid + li, gate=(block["gate"][1], block["gate"][0],
+                                                                       block["up"][0]))
+        else:
+            W, X = gpu_layer(torch, spec, 1000 * wl.wid + li)
+        kind = spec.name.split(".")[1]
+        block[kind] = (W, X)
+        if kind == "down":
+            block = {}
+        layers.append((spec, W, X))
+    return wl, layers
+
+
+def stack_search(awq, torch, peaks, variants=((128, False), (64, False), (128, True)), reps=1):
+    """AWQ over all 224 linears of the stack (statistic + search + pack per layer, one layer
+    after another on one stream, inputs resident): seconds per stack for each (group size,
+    symmetric) variant, layers/s overall and per shape, against the roofline of the direct-form
+    search flops at the measured bf16 peak."""
+    wl, layers = stack_layers(torch)
+    alphas = synth.alpha_grid(wl.n_alpha)
+    out = {"linears": len(layers), "T": layers[0][0].t, "variants": []}
+    direct_total = sum(search_flops(W.shape[0], W.shape[1], X.shape[0], len(alphas), "direct")[0]
+                       for _, W, X in layers)
+    for G, sym in variants:
+        bufs = {}
+        for _, W, X in layers:
+            key = (W.shape[0], W.shape[1])
+            if key not in bufs:
+                bufs[key] = SearchBuffers(awq, torch, W.shape[0], W.shape[1], X.shape[0],
+                                          len(alphas), G, sym)
+        for _, W, X in layers:                                   # warm-up pass
+            enqueue_layer(awq, W, X, alphas, G, sym, bufs[(W.shape[0], W.shape[1])])
+        awq.awq_stream_status()
+        per_shape = {}
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in layers]
+        awq.awq_profile_begin()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(reps):
+            e0.record()
+            for i, (_, W, X) in enumerate(layers):
+                ev[i][0].record()
+                enqueue_layer(awq, W, X, alphas, G, sym, bufs[(W.shape[0], W.shape[1])])
+                ev[i][1].record()
+            e1.record()
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+            for i, (_, W, _x) in enumerate(layers):
+                per_shape.setdefault(f"{W.shape[0]}x{W.shape[1]}", []).append(ev[i][0].elapsed_time(ev[i][1]))
+        prof = awq.awq_profile_end()
+        awq.awq_stream_status()
+        sec = tot / reps / 1e3
+        roof = direct_total / (peaks["bf16_tflops"] * 1e12)
+        sched = schedule_of(prof)
+        n_k, ms_k = prof.get("score", (0, 0.0))
+        score_flops = sum(search_flops(W.shape[0], W.shape[1], X.shape[0], len(alphas), "direct")[0]
+                          for _, W, X in layers) * reps
+        out["variants"].append({
+            "group_size": G, "symmetric": sym, "seconds_per_stack": round(sec, 4),
+            "layers_per_s": round(len(layers) / sec, 1), "schedule": sched,
+            "roofline_s": round(roof, 4), "frac_of_roofline": round(roof / sec, 4),
+            "per_shape_ms": {k: round(sum(v) / len(v), 3) for k, v in per_shape.items()},
+            "scoring_kernel_tflops": round(score_flops / (ms_k * 1e-3) / 1e12, 1) if n_k else None,
+            "kernels_ms": {k: round(v[1] / reps, 2) for k, v in prof.items()}})
+        del bufs
+        torch.cuda.empty_cache()
+    out["direct_form_tflop"] = round(direct_total / 1e12, 1)
+    out["timing"] = ("one pass over all linears after a warm-up pass, layers one after another "
+                     "on one stream, inputs resident in HBM (13 GB of weights, 4.7 GB of "
+                     "calibration activations)")
+    return out, wl, layers
+
+
+def stack_search_e2e(awq, torch, layers, alphas, G=128):
+    """The stack pass through the C ABI from pinned host buffers: every layer's W and X are
+    uploaded and its results (errors, alpha index, scales, packed codes, steps, zero points)
+    read back inside the timed region. Two device buffer sets per shape alternate, with the
+    copies on their own streams (one per direction), as a layer-by-layer pipeline would run.
+    The host side holds one pinned W and X per shape (their values do not change the time)."""
+    host = {}
+    for _, W, X in layers:
+        key = (W.shape[0], W.shape[1])
+        if key not in host:
+            host[key] = (W.cpu().pin_memory(), X.cpu().pin_memory())
+    dev = {}
+    for key, (Wh, Xh) in host.items():
+        dev[key] = [(torch.empty_like(Wh, device="cuda"), torch.empty_like(Xh, device="cuda"),
+                     SearchBuffers(awq, torch, key[0], key[1], Xh.shape[0], len(alphas), G, False))
+                    for _ in range(2)]
+    outs = {key: [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in d[2].outputs()]
+                  for d in dv] for key, dv in dev.items()}
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    state = {key: {"uploaded": [torch.cuda.Event(), torch.cuda.Event()],
+                   "computed": [torch.cuda.Event(), torch.cuda.Event()],
+                   "read": [torch.cuda.Event(), torch.cuda.Event()], "used": [False, False],
+                   "next": 0} for key in dev}
+    h2d = d2h = 0
+
+    def one(key):
+        nonlocal h2d, d2h
+        st = state[key]
+        k = st["next"]
+        st["next"] ^= 1
+        Wd, Xd, b = dev[key][k]
+        Wh, Xh = host[key]
+        with torch.cuda.stream(up):
+            if st["used"][k]:
+                up.wait_event(st["computed"][k])
+            Wd.copy_(Wh, non_blocking=True)
+            Xd.copy_(Xh, non_blocking=True)
+            st["uploaded"][k].record(up)
+        comp.wait_event(st["uploaded"][k])
+        if st["used"][k]:
+            comp.wait_event(st["read"][k])
+        enqueue_layer(awq, Wd, Xd, alphas, G, False, b)
+        st["computed"][k].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(st["computed"][k])
+            for hbuf, o in zip(outs[key][k], b.outputs()):
+                hbuf.copy_(o, non_blocking=True)
+            st["read"][k].record(down)
+        st["used"][k] = True
+        h2d += Wh.numel() * 2 + Xh.numel() * 2
+        d2h += sum(o.numel() * o.element_size() for o in b.outputs())
+
+    for _, W, _x in layers[:14]:                                   # warm-up
+        one((W.shape[0], W.shape[1]))
+    torch.cuda.synchronize()
+    h2d = d2h = 0
+    t0 = time.perf_counter()
+    for _, W, _x in layers:
+        one((W.shape[0], W.shape[1]))
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    awq.awq_stream_status()
+    return {"value": round(len(layers) / dt, 1), "unit": "layers/s", "seconds_per_stack": round(dt, 4),
+            "h2d_bytes_per_stack": h2d, "d2h_bytes_per_stack": d2h, "group_size": G,
+            "pipelining": "two buffer sets per shape; H2D and D2H on their own streams overlap "
+                          "compute; one pinned host W and X per shape"}
+
+
+def stack_cpu_baseline(G=128, budget_s=4.0):
+    """The oracle (statistic, search, pack) on a bounded row slice of one layer of each of the
+    stack's three shapes (host draws, T = 2048), extrapolated linearly in rows and by the shape
+    counts to the 224 linears."""
+    wl = synth.WORKLOADS["llama7b-stack"]
+    alphas = synth.alpha_grid(wl.n_alpha)
+    counts = {}
+    first = {}
+    for li, spec in enumerate(wl.layers):
+        key = (spec.n, spec.k)
+        counts[key] = counts.get(key, 0) + 1
+        first.setdefault(key, li)
+    total = 0.0
+    detail = {}
+    sample = 0.0
+    for key, li in first.items():
+        layer = synth.make_layer("llama7b-stack", li)
+        rows, m = choose_rows(layer, alphas, (), G, budget_s)
+        sec, d = oracle_layer_seconds(layer, alphas, (), G, rows)
+        total += sec * counts[key]
+        sample += d["t_stats"] + d["t_rows"]
+        detail[f"{key[0]}x{key[1]}"] = {"rows": rows, "seconds_per_layer": round(sec, 2),
+                                        "layers": counts[key]}
+    return {"value": round(len(wl.layers) / total, 5), "unit": "layers/s",
+            "seconds_per_stack": round(total, 1), "cores": blas_threads(), "kind": "oracle",
+            "cpu_model": cpu_model(), "per_shape": detail, "sample_seconds": round(sample, 1),
+            "sample": "oracle (fp64 numpy) statistic, 20-alpha search and pack on a row slice of "
+                      "the first layer of each shape of the stack (all T=2048 tokens), time "
+                      "extrapolated linearly in rows and by the number of layers of each shape"}
 
 
 def run_ours(args):
@@ -736,9 +1067,13 @@ def run_ours(args):
         "wall_s_timed": round(t_wall, 4),
     }
     if rank == 0 and not args.no_hbm_sweep:
-        shapes = [(step.N, step.K), (28672, 8192), (8192, 28672)]
-        line["w4a16"] = w4a16_sweep(awq, torch, shapes, sorted(set(step.gemm_m) | {1, 16, 1024}),
-                                    step.G, peaks)
+        # every workload's shapes at its own batch sizes: the benchmark layer (4096^2), the
+        # Llama-7B MLP (4096 <-> 11008) and the Llama-70B MLP (8192 <-> 28672)
+        m7 = sorted(set(step.gemm_m) | {1, 1024})
+        m_mlp = list(synth.WORKLOADS["llama7b-mlp"].gemm_m)
+        m70 = sorted(set(synth.WORKLOADS["llama70b-mlp"].gemm_m) | {2, 4, 16, 128})
+        shapes = [(step.N, step.K), (11008, 4096), (4096, 11008), (28672, 8192), (8192, 28672)]
+        line["w4a16"] = w4a16_sweep(awq, torch, shapes, [m7, m_mlp, m_mlp, m70, m70], step.G, peaks)
         dec = [r for r in line["w4a16"] if r["M"] == 1 and r["N"] == 28672]
         pre = [r for r in line["w4a16"] if r["M"] == 1024 and r["N"] == 28672]
         if dec:
@@ -751,7 +1086,26 @@ def run_ours(args):
                 "bound": "tensor", "kernel": pre[0]["kernel"], "shape": "M=1024, 8192 -> 28672",
                 "achieved": pre[0]["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": pre[0]["frac_tensor"], "traffic": None}
-        line["w4a16_stack_decode"] = stack_decode(awq, torch, peaks)
+        sd = stack_decode(awq, torch, peaks, G=128, ms=tuple(range(1, 65)), reps=3)
+        line["w4a16_stack_decode"] = dict(sd[0], timing="one CUDA graph of all linears, "
+                                                        "weights streamed from HBM")
+        line["w4a16_stack_decode_sweep"] = [{k: r[k] for k in ("M", "ms_per_token_step",
+                                                                "tokens_per_s", "frac_hbm")}
+                                            for r in sd]
+        sd64 = stack_decode(awq, torch, peaks, G=64, ms=(1, 8, 64), reps=3)
+        line["w4a16_stack_decode_g64"] = [{k: r[k] for k in ("M", "ms_per_token_step",
+                                                              "tokens_per_s", "frac_hbm")}
+                                          for r in sd64]
+    if rank == 0 and not args.no_workloads:
+        line["search_layers"] = search_workloads(awq, torch, peaks)
+        stack, swl, slayers = stack_search(awq, torch, peaks)
+        if not args.no_e2e:
+            stack["e2e"] = stack_search_e2e(awq, torch, slayers, synth.alpha_grid(swl.n_alpha))
+        del slayers
+        torch.cuda.empty_cache()
+        if world == 1 and not args.no_cpu_baseline:
+            stack["cpu_baseline"] = stack_cpu_baseline()
+        line["stack_search"] = stack
     if not args.no_e2e:
         line["e2e"] = e2e_run(awq, torch, step, layer, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -370,29 +370,55 @@ awq_status_t gemv_shape(gemv::Args& a, int G, int sms) {
   if (a.parts > gemv::CWARPS) return AWQ_ERR_UNSUPPORTED_SHAPE;
   a.row_groups = gemv::CWARPS / a.parts;
   const int row_bytes = a.K / 2;
-  a.rows_stage = std::max(a.row_groups, (32768 / row_bytes) / a.row_groups * a.row_groups);
-  a.stage_bytes = a.rows_stage * row_bytes;
   a.pstride = a.K / G + 1;
-  // no more stages than the CTA's rows fill (at least 2)
-  const int stages_needed = (a.rows_max + a.rows_stage - 1) / a.rows_stage;
-  auto fit = [&]() {
+  // Group parameters by TMA boxes where the arrays allow it: the rows of a CTA, its start
+  // rounded down to 16, fit one box (at most 256 columns), and the row strides of the steps
+  // (2 N bytes) and zero points (N bytes) are multiples of 16 bytes. The box width is 32 j + 16,
+  // so the 8 groups a warp's lanes read per row fall on distinct banks for the zero points and
+  // on two-way shared banks for the steps.
+  const int ng = a.K / G;
+  const int bc = (a.rows_max + 15 + 15) / 32 * 32 + 16;
+  const bool box_ok = bc <= 256 && a.N % (a.zeros ? 16 : 8) == 0;
+  // Rows per stage: about 32 KB, preferably a multiple of 2 RG (every consumer warp then takes
+  // its rows two at a time), else a multiple of RG. The ring is as deep as shared memory allows
+  // (at least 2 stages, no more than the CTA's rows fill).
+  auto fit = [&](int unit) {
+    a.rows_stage = std::max(unit, (32768 / row_bytes + unit / 2) / unit * unit);
+    a.stage_bytes = a.rows_stage * row_bytes;
+    const int stages_needed = (a.rows_max + a.rows_stage - 1) / a.rows_stage;
     a.nstages = std::max(2, std::min(gemv::MAX_STAGES, stages_needed));
     while (a.nstages > 2 && gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) --a.nstages;
     return gemv::smem_bytes(a) <= static_cast<size_t>(gemv::SMEM_BUDGET);
   };
-  a.x_direct = 0;
-  if (fit()) return AWQ_OK;
-  // The staged activation planes do not fit beside two weight stages (long K with M = 2). With
-  // at most two row groups no two lanes of a CTA share activations, so each lane converts its
-  // own (measured slower where the staged form fits, hence only here).
-  if (a.row_groups > 2) return AWQ_ERR_UNSUPPORTED_SHAPE;
-  a.x_direct = 1;
-  return fit() ? AWQ_OK : AWQ_ERR_UNSUPPORTED_SHAPE;
+  // In order of preference: staged activation planes, then (long K with at most two row groups,
+  // where no two lanes of a CTA share activations) each lane converting its own; parameter
+  // boxes, then plain parameter loads; paired rows, then single rows.
+  for (int direct = 0; direct < 2; ++direct) {
+    if (direct && a.row_groups > 2) break;
+    a.x_direct = direct;
+    for (int box = box_ok ? 1 : 0; box >= 0; --box) {
+      a.pbox_cols = box ? bc : 0;
+      a.pbox_groups = box ? std::min(ng, 256) : 0;
+      if (fit(2 * a.row_groups) || fit(a.row_groups)) return AWQ_OK;
+    }
+  }
+  return AWQ_ERR_UNSUPPORTED_SHAPE;
 }
 
 template <int M>
 awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
   const size_t smem = gemv::smem_bytes(a);
+  // tensor maps of the group parameters [K/G, N] (unused when they are staged by plain loads)
+  CUtensorMap tmS, tmZ;
+  std::memset(&tmS, 0, sizeof(tmS));
+  std::memset(&tmZ, 0, sizeof(tmZ));
+  if (a.pbox_cols) {
+    AWQ_TRY(make_map_plain(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.scales, a.K / G, a.N, a.N,
+                           a.pbox_cols, a.pbox_groups));
+    if (a.zeros)
+      AWQ_TRY(make_map_plain(&tmZ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.zeros, a.K / G, a.N, a.N,
+                             a.pbox_cols, a.pbox_groups));
+  }
   auto kern = G == 128 ? gemv::gemv_kernel<M, 128>
               : G == 64 ? gemv::gemv_kernel<M, 64> : gemv::gemv_kernel<M, 32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -412,7 +438,7 @@ awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_start(AWQ_K_GEMV, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmS, tmZ, a);
   const awq_status_t rl = launched(AWQ_K_GEMV, st);
   return e != cudaSuccess ? AWQ_ERR_CUDA : rl;
 }
