@@ -253,11 +253,17 @@ awq_status_t launch_k(void (*kern)(P...), dim3 grid, int threads, size_t smem, i
 // ------------------------------------------------------------------ launch helpers
 
 awq_status_t launch_calib_stats(const __half* X, int64_t T, int64_t K, int64_t ldx, float* m,
-                                cudaStream_t st) {
+                                const DeviceInfo* d, cudaStream_t st) {
+  // boxes of 128 rows x 64 columns of X (row stride ldx); columns past K and rows past T read
+  // as zero
+  CUtensorMap map;
+  AWQ_TRY(make_map_plain(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, X, T, K, ldx, stats::COLS,
+                         stats::BOX_ROWS));
   dim3 grid(static_cast<unsigned>((K + stats::COLS - 1) / stats::COLS), stats::CLUSTER);
   prof_start(AWQ_K_CALIB_STATS, st);
-  stats::calib_stats_kernel<<<grid, stats::THREADS, 0, st>>>(X, static_cast<int>(T),
-                                                             static_cast<int>(K), ldx, m);
+  stats::calib_stats_kernel<<<grid, stats::THREADS, 0, st>>>(map, static_cast<int>(T),
+                                                             static_cast<int>(K), m, d->status,
+                                                             g_wait_limit_ns.load());
   return launched(AWQ_K_CALIB_STATS, st);
 }
 
@@ -443,12 +449,12 @@ awq_status_t launch_gemv_m(const gemv::Args& a, int G, cudaStream_t st) {
   return e != cudaSuccess ? AWQ_ERR_CUDA : rl;
 }
 
-// Sum of the per-CTA partials of every alpha in a fixed order (one warp per alpha: lane l adds
-// partials l, l + 32, ..., then a fixed butterfly), the 2^-2p of the residual scale and the
-// 1/(T N) of the mean; first minimiser in fp64; copy out s and 1/s of the winner.
+// Sum of the per-CTA partials of every alpha in a fixed order (one warp per alpha, 32 warps:
+// lane l adds partials l, l + 32, ..., then a fixed butterfly), the 2^-2p of the residual scale
+// and the 1/(T N) of the mean; first minimiser in fp64; copy out s and 1/s of the winner.
 // With the Gram schedule (hmax != NULL) the partials hold 2^-h sum_n d^T H' d, i.e. half of
 // 2^-h sum_n d^T H d: the factor 2^(1 + h) restores it.
-__global__ void __launch_bounds__(256) finalize_kernel(const double* partial, int nparts,
+__global__ void __launch_bounds__(1024) finalize_kernel(const double* partial, int nparts,
                                                        int n_alpha, const unsigned int* absmax,
                                                        const unsigned int* hmax,
                                                        double tn, const float* s_grid,
@@ -460,7 +466,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const double* partial, in
   const int p2 = residual_exponent(*absmax);
   const int h = hmax ? 1 + gram::gram_exponent(*hmax) : 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = warp; i < n_alpha; i += 8) {
+  for (int i = warp; i < n_alpha; i += static_cast<int>(blockDim.x >> 5)) {
     double sum = 0.0;
     for (int c0 = lane; c0 < nparts; c0 += 8 * 32) {  // eight loads in flight, added in order
       double v[8];
@@ -563,7 +569,11 @@ int gram_tiles(int64_t K) {  // GRAM mode: row tiles kt = 0..KT-1 take kt / 2 + 
 
 // Whether scoring through H = X^T X takes fewer tensor-core tile steps (one 128 x 256 x 64
 // MMA block each, counted on the most loaded of `sms` CTAs) than the direct X D^T, including
-// forming H once and the transpose of X (converted at about 1.5 MB of traffic per step).
+// forming H once and the transpose of X (converted at about 1.5 MB of traffic per step). The
+// direct count is weighted by 1.2: its residuals run as separate kernels beside the scoring
+// GEMM and slow it down, while the Gram launch builds them in its own spare warps (measured
+// over layers from 256 x 512 to 28672 x 8192 with 64 to 8192 tokens: the weight picks the
+// faster schedule on all but near-equal cases).
 bool gram_pays(int64_t N, int64_t K, int64_t T, int32_t n_alpha, int sms) {
   const int64_t P = sms;
   const int64_t direct_tiles = ((T + 127) / 128) * ((N + 255) / 256);
@@ -580,7 +590,7 @@ bool gram_pays(int64_t N, int64_t K, int64_t T, int32_t n_alpha, int sms) {
   const int64_t Tp = (T + 63) / 64 * 64;
   const double once = static_cast<double>((gram_tiles(K) + P - 1) / P) * (Tp / 64) +
                       4.0 * static_cast<double>(T) * static_cast<double>(K) / 1.5e6;
-  return static_cast<double>(n_alpha) * per_alpha + once < static_cast<double>(n_alpha) * direct;
+  return static_cast<double>(n_alpha) * per_alpha + once < 1.2 * static_cast<double>(n_alpha) * direct;
 }
 
 // The persistent Gram-schedule search (gram_persistent.cuh): one cooperative launch, one CTA per
@@ -779,7 +789,7 @@ awq_status_t awq_calib_stats(const void* X_f16, int64_t T, int64_t K, int64_t ld
   if (!aligned16(X_f16) || !aligned16(mean_abs)) return AWQ_ERR_MISALIGNED;
   DeviceInfo* d = nullptr;
   AWQ_TRY(device_info(&d));
-  return launch_calib_stats(static_cast<const __half*>(X_f16), T, K, ldx, mean_abs,
+  return launch_calib_stats(static_cast<const __half*>(X_f16), T, K, ldx, mean_abs, d,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1002,7 +1012,7 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   // 1. statistic
   const float* mp = mean_abs;
   if (!mp) {
-    AWQ_TRY(launch_calib_stats(X, T, K, K, m, st));
+    AWQ_TRY(launch_calib_stats(X, T, K, K, m, d, st));
     mp = m;
   }
   // GRAM: the scale grid and max|W| (steps 2-3) run on the library's second stream while X^T
@@ -1024,7 +1034,9 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   ga.n_alpha = n_alpha;
   for (int i = 0; i < n_alpha; ++i) ga.alphas[i] = alphas[i];
   prof_start(AWQ_K_SCALE_GRID, ps);
-  scale_grid_kernel<<<static_cast<unsigned>((K * n_alpha + 255) / 256), 256, 0, ps>>>(ga);
+  scale_grid_kernel<<<dim3(static_cast<unsigned>((K + 127) / 128),
+                           static_cast<unsigned>((n_alpha + GRID_ALPHAS - 1) / GRID_ALPHAS)),
+                      128, 0, ps>>>(ga);
   AWQ_TRY(launched(AWQ_K_SCALE_GRID, ps));
   // 3. max |W| for the residual's power-of-two scale
   if (cudaMemsetAsync(absmax, 0, sizeof(unsigned int), ps) != cudaSuccess) {
@@ -1186,7 +1198,7 @@ awq_status_t awq_search_scale(const void* W_f16, int64_t N, int64_t K, const voi
   }
   // 6. errors, argmin, winning scales
   prof_start(AWQ_K_FINALIZE, st);
-  finalize_kernel<<<1, 256, 0, st>>>(partial, use_gram ? ggrid : sgrid, n_alpha, absmax,
+  finalize_kernel<<<1, 1024, 0, st>>>(partial, use_gram ? ggrid : sgrid, n_alpha, absmax,
                                      use_gram ? hmax : nullptr,
                                      static_cast<double>(T) * static_cast<double>(N), s_grid,
                                      inv_grid, static_cast<int>(K), err_out, best_idx, s_out,

@@ -33,24 +33,6 @@ struct GroupParams {
 __device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool symmetric,
                                                       int bits);
 
-// Group step and zero point; TEAM = G / 8 consecutive lanes hold one group.
-template <int TEAM>
-__device__ __forceinline__ GroupParams group_params(const float (&wp)[8], bool symmetric,
-                                                    int bits) {
-  float lo = wp[0], hi = wp[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    lo = fminf(lo, wp[i]);
-    hi = fmaxf(hi, wp[i]);
-  }
-#pragma unroll
-  for (int o = TEAM / 2; o >= 1; o >>= 1) {
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  return group_params_of(lo, hi, symmetric, bits);
-}
-
 // Round to the nearest integer, ties to even, for |x| < 2^22: x + 1.5 * 2^23 lies in a binade
 // whose unit in the last place is 1, so that IEEE addition rounds x itself (1.5 * 2^23 is even,
 // so ties land on even integers) and the subtraction is exact. Two full-rate adds.
@@ -107,7 +89,9 @@ __device__ __forceinline__ GroupParams group_params_of(float lo, float hi, bool 
   return g;
 }
 
-// rint(fl32(wp / step)) without a division in the common case. |wp / step| <= 15 for every
+// The rule every kernel here decides codes by, in its plainest form (the kernels apply it in
+// the shifted domain below, with the same integers): rint(fl32(wp / step)) without a division
+// in the common case. |wp / step| <= 15 for every
 // weight of the group, so t = fl32(wp * fl32(1 / step)) is within 2^-19 of the exact quotient
 // and fl32 of the quotient within 2^-20 of it: unless t lies within 2^-17 of a half-integer (a
 // rounding boundary of rint), t and the IEEE quotient round to the same integer. With
@@ -119,19 +103,6 @@ __device__ __forceinline__ float rint_quotient(float wp, const GroupParams& g) {
   const float r = rint_small(t);
   if (fabsf(__fsub_rn(t, r)) >= 0.5f - 0x1p-17f) return rintf(__fdiv_rn(wp, g.step));
   return r;
-}
-
-// Stored code of one scaled weight, as an exact float: clamp(rint(w' / step) + zero) to the
-// code range (symmetric: zero = 8, so the clamp of q to [-2^(N-1), 2^(N-1) - 1] is shifted by 8).
-__device__ __forceinline__ float code_f(float wp, const GroupParams& g) {
-  const float r = rint_quotient(wp, g);
-  return fminf(fmaxf(__fadd_rn(r, g.zero), g.clo), g.chi);
-}
-
-// The same code as an integer: the low bits of fl32(code + 2^23), whose unit in the last
-// place is 1 (no float-to-integer conversion instruction).
-__device__ __forceinline__ uint32_t code_of(float wp, const GroupParams& g) {
-  return __float_as_uint(__fadd_rn(code_f(wp, g), 0x1p23f)) & 0xFu;
 }
 
 // ------------------------------------------------------------------ quantize + pack kernel
@@ -195,18 +166,62 @@ __global__ void __launch_bounds__(256) quantize_pack_kernel(QuantArgs a) {
                  : make_uint4(0, 0, 0, 0);
   }
   const bool sym = a.symmetric != 0;
+  // The codes in the shifted domain: with C = 1.5 * 2^23 + zero (an integer whose unit in the
+  // last place is 1), u = fl32(w' rcp + C) = C + rint(w' rcp) in one FMA, exactly the integer
+  // rint_quotient gives unless w' rcp - rint(w' rcp) lies within 2^-17 of +-1/2 (checked once
+  // per lane, IEEE division there). The clamped u holds the stored code in its low four bits.
+  // Element pairs go through the paired fp32 instructions (the same IEEE operations).
+  constexpr float kM = 0x1.8p23f;
+  const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
   for (int r = 0; r < QROWS; ++r) {
     const int row = rbase + r;
-    float wv[8], wp[8];
+    float wv[8];
     unpack8(raw[r], wv);
+    float2 v[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wp[i] = a.s ? __fmul_rn(wv[i], sv[i]) : wv[i];
-    const GroupParams g = group_params<TEAM>(wp, sym, a.bits);  // every lane shuffles
+    for (int i = 0; i < 4; ++i) {
+      const float2 w2 = make_float2(wv[2 * i], wv[2 * i + 1]);
+      v[i] = a.s ? mul2_rn(w2, make_float2(sv[2 * i], sv[2 * i + 1])) : w2;
+    }
+    float lo = fminf(v[0].x, v[0].y), hi = fmaxf(v[0].x, v[0].y);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+      lo = fminf(lo, fminf(v[i].x, v[i].y));
+      hi = fmaxf(hi, fmaxf(v[i].x, v[i].y));
+    }
+#pragma unroll
+    for (int o = TEAM / 2; o >= 1; o >>= 1) {   // every lane shuffles
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    const GroupParams g = group_params_of(lo, hi, sym, a.bits);
+    const float c = __fadd_rn(kM, g.zero);
+    const float2 c2 = make_float2(c, c), rcp2 = make_float2(g.rcp, g.rcp);
+    float fmax_abs = 0.0f;
+    float2 u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      u[i] = fma2_rn(v[i], rcp2, c2);
+      const float2 f = fma2_rn(v[i], rcp2, fma2_rn(u[i], m1, c2));
+      fmax_abs = fmaxf(fmax_abs, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+    if (fmax_abs >= 0.5f - 0x1p-17f) {   // see rint_quotient
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        u[i].x = __fadd_rn(rintf(__fdiv_rn(v[i].x, g.step)), c);
+        u[i].y = __fadd_rn(rintf(__fdiv_rn(v[i].y, g.step)), c);
+      }
+    }
+    const float ulo = __fadd_rn(kM, g.clo), uhi = __fadd_rn(kM, g.chi);
     if (wok && row < a.N) {
       uint32_t packed = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) packed |= code_of(wp[i], g) << (4 * i);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c0 = __float_as_uint(fminf(fmaxf(u[i].x, ulo), uhi)) & 0xFu;
+        const uint32_t c1 = __float_as_uint(fminf(fmaxf(u[i].y, ulo), uhi)) & 0xFu;
+        packed |= (c0 | (c1 << 4)) << (8 * i);
+      }
       a.qweight[static_cast<long long>(row) * kw + w] = packed;
       if ((lane & (TEAM - 1)) == 0) {
         const long long gi = static_cast<long long>(k0 / G) * a.N + row;
@@ -219,7 +234,13 @@ __global__ void __launch_bounds__(256) quantize_pack_kernel(QuantArgs a) {
 
 // ------------------------------------------------------------------ search-side kernels
 
-// s[i, k] = fp32(max(m_k, 1e-6)^alpha_i) computed in fp64; inv_s = 1 / s (IEEE fp32).
+// s[i, k] = fp32(max(m_k, 1e-6)^alpha_i) computed in fp64 as 2^(alpha_i log2(base)), the
+// logarithm once per channel; inv_s = 1 / s (IEEE fp32). For base in [1e-6, 2^64], |log2| <= 64,
+// so the fp64 logarithm (1 ulp) and the product with alpha (half an ulp) put the exponent
+// within about 1.5 * 2^-46 of exact, and the power within about 2^-46 relative of
+// max(m, 1e-6)^alpha before its rounding to fp32 (whose spacing is 2^-23): the fp32 scale
+// equals the correctly rounded power except when the power lies that close to a rounding
+// boundary, where it is one fp32 spacing off.
 struct GridArgs {
   const float* m;  // [K]
   float* s;        // [n_alpha, K]
@@ -228,14 +249,23 @@ struct GridArgs {
   float alphas[64];
 };
 
-__global__ void __launch_bounds__(256) scale_grid_kernel(GridArgs a) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= a.K * a.n_alpha) return;
-  const int i = idx / a.K, k = idx - i * a.K;
-  const double base = fmax(static_cast<double>(a.m[k]), 1e-6);
-  const float s = static_cast<float>(pow(base, static_cast<double>(a.alphas[i])));
-  a.s[idx] = s;
-  a.inv_s[idx] = __fdiv_rn(1.0f, s);
+constexpr int GRID_ALPHAS = 4;  // alphas per thread (blockIdx.y picks the chunk)
+
+__global__ void __launch_bounds__(128) scale_grid_kernel(GridArgs a) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= a.K) return;
+  const double lb = log2(fmax(static_cast<double>(a.m[k]), 1e-6));
+  const int i0 = blockIdx.y * GRID_ALPHAS;
+#pragma unroll
+  for (int j = 0; j < GRID_ALPHAS; ++j) {
+    const int i = i0 + j;
+    if (i < a.n_alpha) {
+      const float s = static_cast<float>(exp2(lb * static_cast<double>(a.alphas[i])));
+      const long long idx = static_cast<long long>(i) * a.K + k;
+      a.s[idx] = s;
+      a.inv_s[idx] = __fdiv_rn(1.0f, s);
+    }
+  }
 }
 
 // max |W| over the whole matrix, as the bit pattern of a non-negative float (atomicMax on
@@ -334,20 +364,23 @@ __device__ __forceinline__ void residual_rows(const ResidualArgs& a, const Resid
                                               const float (&sv)[8], const float (&iv)[8],
                                               float p2) {
   const bool sym = a.symmetric != 0;
-  float v[RB][8];  // w', then the rounded quotient rint(w' / step)
+  // Element pairs (2 i, 2 i + 1) go through the paired fp32 instructions (fma2_rn, mul2_rn):
+  // the same IEEE operations as one element at a time, half the instructions.
+  float2 v[RB][4];  // w', then the shifted rounded quotients
   float lo[RB], hi[RB];
 #pragma unroll
   for (int q = 0; q < RB; ++q) {
     float wv[8];
     unpack8(r.raw[q0 + q], wv);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[q][i] = __fmul_rn(wv[i], sv[i]);
-    lo[q] = v[q][0];
-    hi[q] = v[q][0];
+    for (int i = 0; i < 4; ++i)
+      v[q][i] = mul2_rn(make_float2(wv[2 * i], wv[2 * i + 1]), make_float2(sv[2 * i], sv[2 * i + 1]));
+    lo[q] = fminf(v[q][0].x, v[q][0].y);
+    hi[q] = fmaxf(v[q][0].x, v[q][0].y);
 #pragma unroll
-    for (int i = 1; i < 8; ++i) {
-      lo[q] = fminf(lo[q], v[q][i]);
-      hi[q] = fmaxf(hi[q], v[q][i]);
+    for (int i = 1; i < 4; ++i) {
+      lo[q] = fminf(lo[q], fminf(v[q][i].x, v[q][i].y));
+      hi[q] = fmaxf(hi[q], fmaxf(v[q][i].x, v[q][i].y));
     }
   }
 #pragma unroll
@@ -362,32 +395,38 @@ __device__ __forceinline__ void residual_rows(const ResidualArgs& a, const Resid
 #pragma unroll
   for (int q = 0; q < RB; ++q) g[q] = group_params_of(lo[q], hi[q], sym, a.bits);
   // The integers are carried shifted by kM = 1.5 * 2^23, where the unit in the last place is 1:
-  // u = fl32(w' rcp + kM) = kM + rint(w' rcp) in one FMA, and kM - u = -rint(w' rcp) exactly,
-  // so fma(w', rcp, kM - u) is w' rcp - rint(w' rcp) rounded once. Where that lies within
-  // 2^-17 of +-1/2 the exact product w' rcp (within 2^-19 of the quotient, like t in
-  // rint_quotient) may round differently from fl32(w' / step); elsewhere both give rint_quotient's
-  // integer.
+  // u = fl32(w' rcp + kM) = kM + rint(w' rcp) in one FMA, and kM - u = -rint(w' rcp) exactly
+  // (formed as fma(u, -1, kM), the same exact value), so fma(w', rcp, kM - u) is
+  // w' rcp - rint(w' rcp) rounded once. Where that lies within 2^-17 of +-1/2 the exact product
+  // w' rcp (within 2^-19 of the quotient, like t in rint_quotient) may round differently from
+  // fl32(w' / step); elsewhere both give rint_quotient's integer.
   constexpr float kM = 0x1.8p23f;
-  bool edge = false;
+  const float2 kM2 = make_float2(kM, kM), m1 = make_float2(-1.0f, -1.0f);
+  float fmax_abs = 0.0f;
 #pragma unroll
   for (int q = 0; q < RB; ++q) {
+    const float2 rcp2 = make_float2(g[q].rcp, g[q].rcp);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float u = __fmaf_rn(v[q][i], g[q].rcp, kM);
-      edge |= fabsf(__fmaf_rn(v[q][i], g[q].rcp, __fsub_rn(kM, u))) >= 0.5f - 0x1p-17f;
+    for (int i = 0; i < 4; ++i) {
+      const float2 u = fma2_rn(v[q][i], rcp2, kM2);
+      const float2 f = fma2_rn(v[q][i], rcp2, fma2_rn(u, m1, kM2));
+      fmax_abs = fmaxf(fmax_abs, fmaxf(fabsf(f.x), fabsf(f.y)));
       v[q][i] = u;
     }
   }
-  if (edge) {  // see rint_quotient
+  if (fmax_abs >= 0.5f - 0x1p-17f) {  // see rint_quotient
 #pragma unroll
     for (int q = 0; q < RB; ++q) {
       float wv[8];
       unpack8(r.raw[q0 + q], wv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        v[q][i] = __fadd_rn(rintf(__fdiv_rn(__fmul_rn(wv[i], sv[i]), g[q].step)), kM);
+      for (int i = 0; i < 4; ++i) {
+        v[q][i].x = __fadd_rn(rintf(__fdiv_rn(__fmul_rn(wv[2 * i], sv[2 * i]), g[q].step)), kM);
+        v[q][i].y = __fadd_rn(rintf(__fdiv_rn(__fmul_rn(wv[2 * i + 1], sv[2 * i + 1]), g[q].step)), kM);
+      }
     }
   }
+  const float2 p22 = make_float2(p2, p2);
 #pragma unroll
   for (int q = 0; q < RB; ++q) {
     const int row = r.rbase + q0 + q;
@@ -395,25 +434,22 @@ __device__ __forceinline__ void residual_rows(const ResidualArgs& a, const Resid
     const float ulo = __fadd_rn(kM, __fsub_rn(g[q].clo, g[q].zero));
     const float uhi = __fadd_rn(kM, __fsub_rn(g[q].chi, g[q].zero));
     // With sp = step16 p2 (p2 a power of two, so exact): fma(u, sp, -kM sp) = (code - zero) sp
-    // exactly (an integer below 16 times an 11-bit significand), times 1/s rounded once is
-    // fl32((code - zero) step16 / s) p2 = w_hat p2, and fma(w, p2, -w_hat p2) =
+    // exactly (an integer below 16 times an 11-bit significand), times -1/s rounded once is
+    // -fl32((code - zero) step16 / s) p2 = -w_hat p2, and fma(w, p2, -w_hat p2) =
     // fl32(w - w_hat) p2: the same bits as scaling after each rounding.
     const float sp = __fmul_rn(__half2float(__float2half_rn(g[q].step)), p2);
-    const float msp = -__fmul_rn(kM, sp);
+    const float2 sp2 = make_float2(sp, sp);
+    const float2 msp2 = make_float2(-__fmul_rn(kM, sp), -__fmul_rn(kM, sp));
     float wv[8];
     unpack8(r.raw[q0 + q], wv);
     uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      float d2[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float uc = fminf(fmaxf(v[q][i + j], ulo), uhi);
-        const float w_hat_p2 = __fmul_rn(__fmaf_rn(uc, sp, msp), iv[i + j]);
-        d2[j] = __fmaf_rn(wv[i + j], p2, -w_hat_p2);
-      }
-      const __half2 h = __floats2half2_rn(d2[0], d2[1]);
-      memcpy(&out[i / 2], &h, sizeof(uint32_t));
+    for (int i = 0; i < 4; ++i) {
+      const float2 uc = make_float2(fminf(fmaxf(v[q][i].x, ulo), uhi), fminf(fmaxf(v[q][i].y, ulo), uhi));
+      const float2 nwh = mul2_rn(fma2_rn(uc, sp2, msp2), make_float2(-iv[2 * i], -iv[2 * i + 1]));
+      const float2 d = fma2_rn(make_float2(wv[2 * i], wv[2 * i + 1]), p22, nwh);
+      const __half2 h = __floats2half2_rn(d.x, d.y);
+      memcpy(&out[i], &h, sizeof(uint32_t));
     }
     if (r.wok && row < a.N)
       *reinterpret_cast<uint4*>(a.D + static_cast<long long>(row) * a.K + r.k0) =

@@ -128,7 +128,11 @@ def test_host_validation_rejects_without_cuda(L):
         S["AWQ_ERR_MISALIGNED"]
     alphas = (ctypes.c_float * 2)(0.0, 0.5)
     ap = ctypes.cast(alphas, ctypes.c_void_p)
-    ws = awq.awq_search_workspace_bytes(16, 256, 8, 2)
+    awq.awq_set_score_mode("direct")   # the direct schedules' sizes (AUTO may ask for more)
+    try:
+        ws = awq.awq_search_workspace_bytes(16, 256, 8, 2)
+    finally:
+        awq.awq_set_score_mode("auto")
     ws_min = ws - (16 * 256 * 2 + 255) // 256 * 256    # one residual buffer instead of two
     assert _code(L, "awq_search_scale", A, 16, 256, A, 8, None, ap, 2, cfg, A, ws_min, A, A,
                  None, None, None) == S["AWQ_ERR_NO_DEVICE"]    # accepted: only the device check fails

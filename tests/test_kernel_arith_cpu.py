@@ -165,10 +165,12 @@ def _rint_even(fr: Fraction) -> int:
 
 def test_residual_shifted_domain_codes_equal_the_quotient_rule():
     """rint(fl32(w' / step)) without a division, both ways the kernels take it (r = fl32(1/step),
-    kM = 1.5 2^23): the pack kernel rounds t = fl32(w' r) with two adds against kM and checks
-    |t - rint(t)| against 1/2 - 2^-17; the residual forms u = fl32(w' r + kM) in one FMA and checks
-    fl32(w' r + (kM - u)). Past the margin both take the IEEE quotient. In exact arithmetic, on
-    quotients concentrated near the rounding boundaries, both give the defined integer."""
+    kM = 1.5 2^23): the residual forms u = fl32(w' r + kM) in one FMA and checks
+    fl32(w' r + (kM - u)); the pack kernel does the same against C = kM + z for the group's zero
+    point z (an integer, so the code comes out as u - kM); the plain form rounds t = fl32(w' r)
+    with two adds against kM and checks |t - rint(t)|. The margin is 1/2 - 2^-17; past it every
+    form takes the IEEE quotient. In exact arithmetic, on quotients concentrated near the
+    rounding boundaries, all give the defined integer."""
     kM = Fraction(3 * 2 ** 22)
     margin = Fraction(1, 2) - Fraction(1, 2 ** 17)
     rng = np.random.Generator(np.random.PCG64(9))
@@ -192,7 +194,13 @@ def test_residual_shifted_domain_codes_equal_the_quotient_rule():
         else:
             got = int(u - kM)
         assert got == want, (float(wp), float(step))
-        t = _rn32_signed(wp * r)                        # the pack kernel's rule
+        z = int(rng.integers(0, 16))                    # the pack kernel's shifted form
+        c = kM + z
+        up = _rn32_signed(wp * r + c)
+        ep = _rn32_signed(wp * r + (c - up))
+        got_shift = _rint_even(_rn32_signed(wp / step)) if abs(ep) >= margin else int(up - c)
+        assert got_shift == want, (float(wp), float(step), z)
+        t = _rn32_signed(wp * r)                        # the plain form
         rt = _rn32_signed(_rn32_signed(t + kM) - kM)
         got_pack = _rint_even(_rn32_signed(wp / step)) if abs(_rn32_signed(t - rt)) >= margin \
             else int(rt)

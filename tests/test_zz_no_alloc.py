@@ -35,19 +35,25 @@ def _outputs(n_alpha, K):
             torch.full((K,), float("nan"), dtype=torch.float32, device="cuda"))
 
 
-# tiny-512 and the ragged layer take the direct scoring with two residual buffers; the third
-# has more calibration tokens than twice its input channels, so both entry points score through
-# H = X^T X in the persistent launch, whose cross-CTA counters, X^T and H's triangle then live
-# in the static array
+# AUTO scores these layers through H = X^T X in the persistent launch, whose cross-CTA
+# counters, X^T and H's triangle then live in the static array; forced to the direct scoring,
+# both entry points take two residual buffers and the second stream
 CASES = {
     "tiny-512": lambda: synth.make_layer("tiny-512"),
     "ragged": lambda: synth.random_layer(11, 1000, 2048, 300, n_out=10),
-    "gram": lambda: synth.random_layer(12, 2048, 1024, 4096, n_out=10),
+    "long-calibration": lambda: synth.random_layer(12, 2048, 1024, 4096, n_out=10),
 }
 
 
+@pytest.fixture(params=["auto", "direct"])
+def score_mode(request):
+    awq.awq_set_score_mode(request.param)
+    yield request.param
+    awq.awq_set_score_mode("auto")
+
+
 @pytest.mark.parametrize("which", sorted(CASES))
-def test_static_search_matches_workspace_search_on_two_calls(which):
+def test_static_search_matches_workspace_search_on_two_calls(which, score_mode):
     d = CASES[which]()
     W = torch.from_numpy(d["W"]).cuda()
     X = torch.from_numpy(d["X"]).cuda()
@@ -66,7 +72,7 @@ def test_static_search_matches_workspace_search_on_two_calls(which):
         if call == 1:   # the first call may load the library's device code; later ones allocate nothing
             assert torch.cuda.mem_get_info()[0] == free_before
         for name, u, v in zip(("err", "best", "s", "inv_s"), want, got):
-            assert torch.equal(u, v), (which, call, name)
+            assert torch.equal(u, v), (which, score_mode, call, name)
         assert np.all(np.isfinite(got[0].cpu().numpy()))
 
 
