@@ -385,8 +385,9 @@ awq_status_t gemv_shape(gemv::Args& a, int G, int sms) {
   const int ng = a.K / G;
   const int bc = (a.rows_max + 15 + 15) / 32 * 32 + 16;
   const bool box_ok = bc <= 256 && a.N % (a.zeros ? 16 : 8) == 0;
-  // Rows per stage: about 32 KB, preferably a multiple of 2 RG (every consumer warp then takes
-  // its rows two at a time), else a multiple of RG. The ring is as deep as shared memory allows
+  // Rows per stage: about 32 KB, for M = 1 preferably a multiple of 2 RG (every consumer warp
+  // then takes its rows two at a time; with more tokens the registers go to them instead), else
+  // a multiple of RG. The ring is as deep as shared memory allows
   // (at least 2 stages, no more than the CTA's rows fill).
   auto fit = [&](int unit) {
     a.rows_stage = std::max(unit, (32768 / row_bytes + unit / 2) / unit * unit);
@@ -396,19 +397,29 @@ awq_status_t gemv_shape(gemv::Args& a, int G, int sms) {
     while (a.nstages > 2 && gemv::smem_bytes(a) > static_cast<size_t>(gemv::SMEM_BUDGET)) --a.nstages;
     return gemv::smem_bytes(a) <= static_cast<size_t>(gemv::SMEM_BUDGET);
   };
-  // In order of preference: staged activation planes, then (long K with at most two row groups,
-  // where no two lanes of a CTA share activations) each lane converting its own; parameter
-  // boxes, then plain parameter loads; paired rows, then single rows.
-  for (int direct = 0; direct < 2; ++direct) {
-    if (direct && a.row_groups > 2) break;
+  // Parameter boxes before plain parameter loads, paired rows before single rows.
+  auto fit_any = [&](int direct) {
     a.x_direct = direct;
     for (int box = box_ok ? 1 : 0; box >= 0; --box) {
       a.pbox_cols = box ? bc : 0;
       a.pbox_groups = box ? std::min(ng, 256) : 0;
-      if (fit(2 * a.row_groups) || fit(a.row_groups)) return AWQ_OK;
+      if ((a.M == 1 && fit(2 * a.row_groups)) || fit(a.row_groups)) return true;
     }
+    return false;
+  };
+  // Activation planes staged once per CTA, unless K is long enough that they leave fewer than
+  // four ring stages: then, where at most two row groups share a lane's activations, each lane
+  // converts its own (twice the conversion work at worst, but 2 M K bytes of shared memory go
+  // to the weight ring), if that puts more weight bytes in flight.
+  const bool staged = fit_any(0);
+  if (staged && (a.nstages >= 4 || a.row_groups > 2)) return AWQ_OK;
+  if (a.row_groups <= 2) {
+    const gemv::Args keep = a;
+    if (fit_any(1) && (!staged || a.nstages * a.stage_bytes > keep.nstages * keep.stage_bytes))
+      return AWQ_OK;
+    a = keep;
   }
-  return AWQ_ERR_UNSUPPORTED_SHAPE;
+  return staged ? AWQ_OK : AWQ_ERR_UNSUPPORTED_SHAPE;
 }
 
 template <int M>

@@ -113,7 +113,7 @@ __host__ __device__ inline size_t xitem_bytes(const Args& a) {
 __host__ __device__ inline size_t smem_bytes(const Args& a) {
   return static_cast<size_t>(a.nstages) * a.stage_bytes + xs_bytes(a) + xitem_bytes(a) + 128 +
          static_cast<size_t>(param_words(a)) * 4 + static_cast<size_t>(ysum_floats(a)) * 4 +
-         (2 * MAX_STAGES + 2) * 8 + 16;
+         (2 * MAX_STAGES + 1) * 8 + 16;
 }
 
 __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
@@ -151,8 +151,7 @@ __device__ __forceinline__ void stage_params(const Args& a, uint32_t* prm, int r
 // word w of 32 consecutive items reads 512 contiguous bytes (no bank conflict). The item's sum
 // of x_int and 2^(e - 15) go to xsum / xsc.
 template <int M>
-__device__ __forceinline__ void stage_x(const Args& a, uint32_t* xs, int* xsum, float* xsc,
-                                        uint64_t* issued) {
+__device__ __forceinline__ void stage_x(const Args& a, uint32_t* xs, int* xsum, float* xsc) {
   constexpr int U = 4;                      // slots per thread whose loads are in flight together
   const int wpt = a.K / 8;                  // words (slots) per token
   const int items = a.K / ITEM_CH;
@@ -175,11 +174,6 @@ __device__ __forceinline__ void stage_x(const Args& a, uint32_t* xs, int* xsum, 
         ia[u] = make_float4(1.f, 1.f, 1.f, 1.f);
         ib[u] = ia[u];
       }
-    }
-    if (issued != nullptr) {   // the warp's first loads are out: the weight stream may start
-      __syncwarp();
-      if (lane == 0) mbar_arrive(issued);
-      issued = nullptr;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -230,7 +224,6 @@ __device__ __forceinline__ void stage_x(const Args& a, uint32_t* xs, int* xsum, 
       }
     }
   }
-  if (issued != nullptr && lane == 0) mbar_arrive(issued);   // a warp with no slots
 }
 
 // The same conversion done by one lane for one whole item it owns (long K: every lane's items
@@ -340,17 +333,19 @@ __device__ __forceinline__ void row_pass(const Args& a, const uint8_t* stage, ui
         }
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          uint32_t lo = 0u;
-          int hi = 0;
+          // four independent chains of four DP4A (even / odd nibbles, low / high planes), so
+          // consecutive instructions do not wait on each other's results
+          uint32_t lo0 = 0u, lo1 = 0u;
+          int hi0 = 0, hi1 = 0;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            lo = dp4a_uu(ev[v], xr[m][u][4 * v + 0], lo);
-            lo = dp4a_uu(od[v], xr[m][u][4 * v + 1], lo);
-            hi = dp4a_ss(ev[v], xr[m][u][4 * v + 2], hi);
-            hi = dp4a_ss(od[v], xr[m][u][4 * v + 3], hi);
+            lo0 = dp4a_uu(ev[v], xr[m][u][4 * v + 0], lo0);
+            lo1 = dp4a_uu(od[v], xr[m][u][4 * v + 1], lo1);
+            hi0 = dp4a_ss(ev[v], xr[m][u][4 * v + 2], hi0);
+            hi1 = dp4a_ss(od[v], xr[m][u][4 * v + 3], hi1);
           }
           // sum (q - z) x_int, exact: |.| < 32 * 15 * 2^15 < 2^24, so the float is exact too
-          const int t = hi * 256 + static_cast<int>(lo) - z * sx[m][u];
+          const int t = (hi0 + hi1) * 256 + static_cast<int>(lo0 + lo1) - z * sx[m][u];
           acc[h][m] = fmaf(static_cast<float>(t), step * sc[m][u], acc[h][m]);
         }
       }
@@ -387,8 +382,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(ysum + ysum_floats(a));
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* pbar = empty + MAX_STAGES;          // the parameter boxes
-  uint64_t* xissued = pbar + 1;                 // every consumer warp has issued its x loads
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(xissued + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(pbar + 1);
   // TMA parameter boxes: fp16 steps [boxes * pbox_groups][pbox_cols], then (asymmetric) the
   // uint8 zero points in the same shape, 128-byte aligned; column c of a box is output row
   // x0 + c, x0 = r0 rounded down to 16
@@ -410,7 +404,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&empty[s], CWARPS);
     }
     mbar_init(pbar, 1);
-    mbar_init(xissued, CWARPS);
     *abort_flag = 0;
     fence_mbar_init();
     if (a.pbox_cols) {
@@ -445,10 +438,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (; j < nstage_total; ++j) {
         const int s = j % a.nstages;
         const uint32_t ph = (j / a.nstages) & 1u;
-        // After the first stage the stream waits until every consumer warp has issued its
-        // activation loads: those are on the critical path of every CTA and would otherwise
-        // queue behind the whole ring's worth of weight reads of all CTAs.
-        if (j == 1 && !a.x_direct && !wait_bounded(xissued, 0, wc)) { ok = false; break; }
         if (!wait_bounded(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
         const int row_lo = r0 + j * a.rows_stage;
         const uint32_t bytes = static_cast<uint32_t>(min(a.rows_stage, r1 - row_lo)) * row_bytes;
@@ -473,7 +462,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // Activations (and the output) may belong to the previous kernel of the stream: everything
   // below waits for it. The weight stream and the group parameters above do not.
   pdl_wait();
-  if (!a.x_direct) stage_x<M>(a, xs, xsum, xsc, xissued);
+  if (!a.x_direct) stage_x<M>(a, xs, xsum, xsc);
   named_bar_sync(1, CTHREADS);
   bool ok = true;
   if (a.pbox_cols) ok = wait_bounded(pbar, 0, wc);
