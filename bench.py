@@ -539,6 +539,16 @@ class LayerStep:
             [self.ym[M] for M in self.gemm_m]
 
 
+def w4a16_kernel_name(M, K, G):
+    """Which W4A16 kernel the library runs for M tokens and K input channels: the CUDA-core
+    GEMV up to 4 tokens where its K parts fit its 15 consumer warps, the grouped tensor-core
+    kernel up to 16 tokens (G >= 64), the dequant tensor-core kernel otherwise."""
+    ipl = 4 if M == 1 else (2 if M == 2 else 1)
+    if M <= 4 and -(-(K // 32) // (32 * ipl)) <= 15:
+        return "gemv"
+    return "grouped_tc" if M <= 16 and G >= 64 else "dequant_tc"
+
+
 def w4a16_graph_time(awq, torch, N, K, G, M, sets, inv, reps_outer=3):
     """Per-launch time (us) of awq_w4a16_gemm at [M, K] x [N, K]^T, from a CUDA graph that walks
     rotating weight sets (more bytes than L2, so each launch streams its weights from HBM):
@@ -592,7 +602,7 @@ def w4a16_sweep(awq, torch, shapes, ms, G, peaks):
             gbs = byts / (us * 1e-6) / 1e9
             tfl = 2 * M * N * K / (us * 1e-6) / 1e12
             out.append({"N": N, "K": K, "M": M,
-                        "kernel": "gemv" if M <= 2 else ("grouped_tc" if M <= 16 else "dequant_tc"),
+                        "kernel": w4a16_kernel_name(M, K, G),
                         "us": round(us, 3), "GB/s": round(gbs, 1),
                         "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
                         "TFLOP/s": round(tfl, 2),

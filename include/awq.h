@@ -193,9 +193,10 @@ awq_status_t awq_quant_residual(const void* W_f16, int64_t N, int64_t K, const f
 /*
  * W4A16 dequant-fused matmul: Y [M, N] fp16 = X [M, K] fp16 @ (dequant(Q) diag(inv_s))^T,
  * fp32 accumulation. inv_s [K] fp32 or NULL (1/s already folded into the previous layer).
- * M <= 2 runs a CUDA-core GEMV (integer inner products on block fixed-point activations);
- * 3 <= M <= 16 with G >= 64 the tcgen05 grouped kernel; every other M the tcgen05 dequant
- * kernel. With inv_s,
+ * M <= 4 runs a CUDA-core GEMV (integer inner products on block fixed-point activations)
+ * where its K parts fit its 15 consumer warps and its shared memory (K up to 61440, 30720 and
+ * 15360 channels at M = 1, 2 and 3-4); otherwise M <= 16 with G >= 64 the tcgen05 grouped
+ * kernel, and every other M the tcgen05 dequant kernel. With inv_s,
  * X * inv_s must stay inside the fp16 range (as the folded activation would).
  */
 awq_status_t awq_w4a16_gemm(const void* X_f16, int64_t M, int64_t N, int64_t K,
@@ -293,7 +294,7 @@ typedef enum {
   AWQ_K_SCORE = 4,       /* search, DIRECT: tcgen05 sum of squares of X D^T of one alpha */
   AWQ_K_FINALIZE = 5,    /* search: errors, argmin, winning scales */
   AWQ_K_QUANTIZE_PACK = 6,
-  AWQ_K_GEMV = 7,        /* awq_w4a16_gemm, CUDA-core kernel for M <= 2 */
+  AWQ_K_GEMV = 7,        /* awq_w4a16_gemm, CUDA-core kernel for M <= 4 */
   AWQ_K_GEMM_TC = 8,     /* awq_w4a16_gemm, tcgen05 kernels for larger M */
   AWQ_K_GRAM_PREP = 9,   /* search, GRAM: X^T, column sums of squares and their maximum */
   AWQ_K_GRAM = 10,       /* search, GRAM_LAUNCHES: tcgen05 lower triangle of H = X^T X, fp16 */

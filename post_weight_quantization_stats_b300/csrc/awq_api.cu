@@ -1248,7 +1248,10 @@ awq_status_t awq_w4a16_gemm(const void* X_f16, int64_t M, int64_t N, int64_t K,
     a.status = d->status;
     a.limit_ns = g_wait_limit_ns.load();
     if (gemv_shape(a, G, d->sms) == AWQ_OK)
-      return M == 1 ? launch_gemv_m<1>(a, G, st) : launch_gemv_m<2>(a, G, st);
+      return M == 1   ? launch_gemv_m<1>(a, G, st)
+             : M == 2 ? launch_gemv_m<2>(a, G, st)
+             : M == 3 ? launch_gemv_m<3>(a, G, st)
+                      : launch_gemv_m<4>(a, G, st);
   }
   w4tc::Args a{};
   a.Q = qweight;

@@ -1,4 +1,4 @@
-// W4A16 decode GEMV (M <= 2 tokens) on the CUDA cores.
+// W4A16 decode GEMV (M <= 4 tokens) on the CUDA cores.
 //
 // "AWQ > Benefits and Practical Considerations": decode is bound by reading the weights from
 // HBM; the kernel unpacks the 4-bit integers, applies the group scale and zero point and,
@@ -52,12 +52,12 @@ constexpr int CWARPS = 15;                // consumer warps (16 warps in all: 12
 constexpr int CTHREADS = CWARPS * 32;
 constexpr int THREADS = CTHREADS + 32;    // + one producer warp
 constexpr int ITEM_CH = 32;               // channels of one lane item (4 packed words)
-constexpr int MAX_M = 2;
+constexpr int MAX_M = 4;
 constexpr int MAX_STAGES = 8;
 constexpr int SMEM_BUDGET = 220 * 1024;
 
-// Items per lane for M tokens: the registers holding x~ stay at 64 per thread.
-__host__ __device__ constexpr int items_per_lane(int M) { return M == 1 ? 4 : 2; }
+// Items per lane for M tokens: the registers holding x~ stay at 64 per thread or below.
+__host__ __device__ constexpr int items_per_lane(int M) { return M == 1 ? 4 : (M == 2 ? 2 : 1); }
 
 struct Args {
   const __half* X;        // [M, K]
