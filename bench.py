@@ -1085,12 +1085,21 @@ def run_ours(args):
         shapes = [(step.N, step.K), (11008, 4096), (4096, 11008), (28672, 8192), (8192, 28672)]
         line["w4a16"] = w4a16_sweep(awq, torch, shapes, [m7, m_mlp, m_mlp, m70, m70], step.G, peaks)
         dec = [r for r in line["w4a16"] if r["M"] == 1 and r["N"] == 28672]
+        dec_down = [r for r in line["w4a16"] if r["M"] == 1 and r["N"] == 8192 and r["K"] == 28672]
         pre = [r for r in line["w4a16"] if r["M"] == 1024 and r["N"] == 28672]
+        gemv_src = ("w4a16_gemv.cuh",)
         if dec:
             line["roofline_w4a16_decode"] = {
                 "bound": "hbm", "kernel": dec[0]["kernel"], "shape": "M=1, 8192 -> 28672",
                 "achieved": dec[0]["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": dec[0]["frac_hbm"], "traffic": None}
+                "frac": dec[0]["frac_hbm"],
+                "traffic": profiled_traffic("w4a16_gemv_llama70b_up_m1.md", gemv_src)}
+        if dec_down:
+            line["roofline_w4a16_decode_down"] = {
+                "bound": "hbm", "kernel": dec_down[0]["kernel"], "shape": "M=1, 28672 -> 8192",
+                "achieved": dec_down[0]["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dec_down[0]["frac_hbm"],
+                "traffic": profiled_traffic("w4a16_gemv_llama70b_down_m1.md", gemv_src)}
         if pre:
             line["roofline_w4a16_gemm"] = {
                 "bound": "tensor", "kernel": pre[0]["kernel"], "shape": "M=1024, 8192 -> 28672",
