@@ -42,6 +42,11 @@ Readings where the pages are silent (each is listed in the design notes):
   no normalisation of s; ties in the argmin go to the smallest alpha.
 * The error is the mean over all T x C_out outputs of the squared difference between the
   exact output of the fp16 inputs and the output of the dequantised weights.
+* Per-group clipping (the pages print no clipping step; "AWQ Math", "CPU-SLM implications and
+  common pitfalls" only warns to watch the group size): each group's magnitudes are bounded by
+  c max|w'| for a ratio c from a grid (1, 0.95, ..., 0.55), and each group takes the first ratio
+  minimising its own output error on the calibration set with the cross-channel terms dropped,
+  sum_k h_k (W - w_hat)^2 with h_k = sum_t x_tk^2.
 
 Packed format: nibble i (bits 4i..4i+3) of ``qweight[n, w]`` is the code of input channel
 ``k = 8 w + i``; ``scales[g, n]`` (fp16) and ``zeros[g, n]`` (uint8) are per group g of
@@ -101,8 +106,14 @@ def scaled_weight(W: np.ndarray, s) -> np.ndarray:
 
 
 def quantize(W: np.ndarray, s=None, group_size: int = 128, symmetric: bool = False,
-             bits: int = 4) -> dict:
+             bits: int = 4, clip=None) -> dict:
     """Quantise W diag(s) group-wise to ``bits``-wide codes (N in "Weight-only quantization").
+
+    ``clip`` (optional, [N, K/G] fp32 ratios in (0, 1]) bounds each group's magnitudes before
+    the step is taken: with b = fl32(c max|w'|), the asymmetric ends (already widened to hold 0)
+    become min(hi, b) and max(lo, -b), the symmetric max|w'| becomes b; weights outside the
+    bounded range take the end codes through the usual clamp. ``clip`` of all ones is the plain
+    quantiser.
 
     Returns ``codes`` [N, K] (stored nibble values), ``step32`` [N, K/G] (fp32 step the codes
     were decided with), ``step16`` [N, K/G] (stored fp16 step), ``zero`` [N, K/G] (uint8; 8 in
@@ -117,8 +128,12 @@ def quantize(W: np.ndarray, s=None, group_size: int = 128, symmetric: bool = Fal
     if K % group_size:
         raise ValueError("K must be a multiple of the group size")
     grp = wp.reshape(N, K // group_size, group_size)
+    c = None if clip is None else np.asarray(clip, dtype=np.float32).astype(np.float64)
+    bound = None if c is None else fl32(np.max(np.abs(grp), axis=2) * c).astype(np.float64)
     if symmetric:
         amax = np.max(np.abs(grp), axis=2)
+        if c is not None:
+            amax = bound
         step = fl32(amax / half).astype(np.float64)
         step[step == 0.0] = 1.0
         r = np.rint(fl32(grp / step[:, :, None]).astype(np.float64))
@@ -129,6 +144,9 @@ def quantize(W: np.ndarray, s=None, group_size: int = 128, symmetric: bool = Fal
     else:
         hi = np.maximum(np.max(grp, axis=2), 0.0)
         lo = np.minimum(np.min(grp, axis=2), 0.0)
+        if c is not None:
+            hi = np.minimum(hi, bound)
+            lo = np.maximum(lo, -bound)
         rng_ = fl32(hi - lo).astype(np.float64)
         step = fl32(rng_ / qmax).astype(np.float64)
         step[step == 0.0] = 1.0
@@ -171,10 +189,11 @@ def unpack_nibbles(qweight: np.ndarray) -> np.ndarray:
 
 
 def quantize_pack(W: np.ndarray, s=None, group_size: int = 128,
-                  symmetric: bool = False, bits: int = 4) -> dict:
+                  symmetric: bool = False, bits: int = 4, clip=None) -> dict:
     """The stored form: ``qweight`` [N, K/8] uint32, ``scales`` [K/G, N] fp16,
-    ``zeros`` [K/G, N] uint8 (all 8 in symmetric mode), plus the :func:`quantize` details."""
-    qd = quantize(W, s, group_size, symmetric, bits)
+    ``zeros`` [K/G, N] uint8 (all 8 in symmetric mode), plus the :func:`quantize` details.
+    ``clip`` as in :func:`quantize`, [N, K/G]."""
+    qd = quantize(W, s, group_size, symmetric, bits, clip)
     qd["qweight"] = pack_nibbles(qd["codes"])
     qd["scales"] = np.ascontiguousarray(qd["step16"].T)
     qd["zeros"] = np.ascontiguousarray(qd["zero"].T)
@@ -268,6 +287,53 @@ def residual_exponent(W: np.ndarray) -> int:
         return 0
     _, e = np.frexp(mx)            # mx = f 2^e, f in [0.5, 1)
     return 14 - int(e)
+
+
+# ----------------------------------------------------------------------------------------
+# Per-group clipping search (a reading: the pages print no clipping step; see the notes)
+# ----------------------------------------------------------------------------------------
+
+def clip_ratio_grid(n: int = 10) -> np.ndarray:
+    """Clip ratios c_j = 1 - j/20 for j < n (1, 0.95, ..., 0.55 for n = 10) as fp32."""
+    return (1.0 - np.arange(n, dtype=np.float64) / 20.0).astype(np.float32)
+
+
+def channel_energy(X: np.ndarray) -> np.ndarray:
+    """h_k = sum_t X[t, k]^2 in fp64: the calibration energy of input channel k, the weight a
+    weight error on that channel carries in the layer's output error (the diagonal of X^T X)."""
+    X64 = np.asarray(X, dtype=np.float64)
+    h = np.zeros(X64.shape[1], dtype=np.float64)
+    for t in range(X64.shape[0]):
+        h += X64[t] * X64[t]
+    return h
+
+
+def clip_search(W: np.ndarray, X: np.ndarray, s, ratios, group_size: int = 128,
+                symmetric: bool = False, bits: int = 4, h=None) -> dict:
+    """Each group's clip ratio: for every ratio c of ``ratios`` the group is quantised with its
+    range shrunk by c (:func:`quantize`), and its error e(c) = sum_k h_k (W[n, k] - w_hat[n, k])^2
+    over the group's channels k is the group's output error on the calibration set with the
+    cross-channel terms dropped (h = :func:`channel_energy`, w_hat = Q(W diag(s)) diag(s)^-1 as in
+    the search). The first minimiser wins, so with ratios[0] = 1 a group is clipped only when
+    that strictly lowers its error.
+
+    Returns ``best`` [N, K/G] (index into ratios), ``clip`` [K/G, N] fp32 (the chosen ratios,
+    stored like the steps) and ``err`` [n_ratio, N, K/G] (fp64)."""
+    W64 = np.asarray(W, dtype=np.float64)
+    N, K = W64.shape
+    ng = K // group_size
+    if h is None:
+        h = channel_energy(X)
+    h = np.asarray(h, dtype=np.float64)
+    r = np.asarray(ratios, dtype=np.float32)
+    err = np.zeros((len(r), N, ng), dtype=np.float64)
+    for j, c in enumerate(r):
+        clip = np.full((N, ng), c, dtype=np.float32)
+        qd = quantize_pack(W, s, group_size, symmetric, bits, clip=clip)
+        d = W64 - dequantize(qd["qweight"], qd["scales"], qd["zeros"], group_size, s=s)
+        err[j] = (d * d * h[None, :]).reshape(N, ng, group_size).sum(axis=2)
+    best = np.argmin(err, axis=0)                   # numpy returns the first minimiser
+    return {"best": best, "clip": np.ascontiguousarray(r[best].T), "err": err}
 
 
 # ----------------------------------------------------------------------------------------

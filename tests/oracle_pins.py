@@ -459,4 +459,80 @@ def pin_memory_footprint(o):
         assert 3.7 < fp16_gb / q_gb < 4.0
 
 
+# ------------------------------------------------------------------ per-group clipping
+
+def pin_channel_energy(o):
+    """h_k = sum_t x_tk^2: X[t, k] = (t + 1) (k + 1) gives (k + 1)^2 T (T + 1)(2T + 1) / 6."""
+    T, K = 9, 6
+    X = (np.arange(1, T + 1)[:, None] * np.arange(1, K + 1)[None, :]).astype(np.float64)
+    want = (np.arange(1, K + 1) ** 2) * T * (T + 1) * (2 * T + 1) / 6
+    assert np.array_equal(o.channel_energy(X), want)
+
+
+def pin_clip(o):
+    """Clipping (a reading; the pages print no clipping step): a ratio of one is the plain
+    quantiser; a ratio c bounds the group's magnitudes by b = fl32(c max|w'|) (asymmetric range
+    min(hi, b), max(lo, -b); symmetric max|w'| -> b), the weights beyond take the end codes and
+    the rest stay within half the (smaller) step; the search clips deep (to the grid's last
+    ratio) a group whose one large weight sits on a channel with little calibration energy and
+    at most lightly (c >= 0.9) when that channel carries the energy, and with no energy at all
+    every ratio ties and the first (1.0) wins."""
+    rng = np.random.Generator(np.random.PCG64(33))
+    N, K, G = 3, 256, 128
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    grid = o.clip_ratio_grid(10)
+    assert np.array_equal(grid, np.float32([1, .95, .9, .85, .8, .75, .7, .65, .6, .55]))
+    ones = np.ones((N, K // G), np.float32)
+    for sym in (False, True):
+        a, b = o.quantize_pack(W, None, G, sym), o.quantize_pack(W, None, G, sym, clip=ones)
+        for key in ("qweight", "scales", "zeros"):
+            assert np.array_equal(a[key], b[key])
+    # range ends and the half-step bound under a clip of 0.5 (asymmetric)
+    c = np.full((N, K // G), 0.5, np.float32)
+    q = o.quantize(W, None, G, False, clip=c)
+    grp = q["scaled"].reshape(N, K // G, G)
+    b = o.fl32(np.abs(grp).max(axis=2) * 0.5).astype(np.float64)
+    hi = np.minimum(np.maximum(grp.max(axis=2), 0), b)
+    lo = np.maximum(np.minimum(grp.min(axis=2), 0), -b)
+    assert np.all((hi == b) | (lo == -b))         # the larger end is cut to the bound
+    step = q["step32"].astype(np.float64)
+    assert np.array_equal(step, o.fl32(o.fl32(hi - lo) / 15).astype(np.float64))
+    codes = q["codes"].reshape(N, K // G, G).astype(np.float64)
+    w_hat = (codes - q["zero"][:, :, None]) * step[:, :, None]
+    clamped = q["clamped"].reshape(N, K // G, G)
+    free = ~clamped
+    assert np.all(np.abs(grp - w_hat)[free] <= step[:, :, None].repeat(G, 2)[free] / 2 * (1 + 2.0 ** -20))
+    above, below = grp > hi[:, :, None] + step[:, :, None], grp < lo[:, :, None] - step[:, :, None]
+    assert above.any() and below.any()
+    assert np.all(codes[above] == 15) and np.all(clamped[above])
+    assert np.all(codes[below] == 0) and np.all(clamped[below])
+    # the energy decides: one large weight on channel 5 of group 0 of row 0
+    W2 = (rng.uniform(-0.1, 0.1, (1, G))).astype(np.float16)
+    W2[0, 5] = 1.0
+    X = rng.standard_normal((64, G)).astype(np.float16)
+    for h5, deep in ((1e-4, True), (1e4, False)):
+        h = np.ones(G)
+        h[5] = h5
+        r = o.clip_search(W2, X, None, grid, G, h=h)
+        c = grid[r["best"][0, 0]]
+        assert (c == grid[-1]) if deep else (c >= 0.9), (h5, r["err"][:, 0, 0])
+        assert r["err"][r["best"][0, 0], 0, 0] <= r["err"][0, 0, 0]
+        assert r["clip"].shape == (1, 1) and r["clip"][0, 0] == grid[r["best"][0, 0]]
+    rz = o.clip_search(W, X[:, :1].repeat(K, 1), None, grid, G, h=np.zeros(K))
+    assert np.all(rz["best"] == 0) and np.all(rz["clip"] == 1.0)
+    # e(c) is the energy-weighted squared weight error of the group (a brute-force sum)
+    h = rng.uniform(0.5, 2.0, K)
+    r = o.clip_search(W, None, None, grid[:3], G, h=h)
+    for j, cj in enumerate(grid[:3]):
+        qd = o.quantize_pack(W, None, G, False, clip=np.full((N, K // G), cj, np.float32))
+        wh = o.dequantize(qd["qweight"], qd["scales"], qd["zeros"], G)
+        for n in range(N):
+            for g in range(K // G):
+                e = 0.0
+                for k in range(g * G, (g + 1) * G):
+                    d = float(W[n, k]) - wh[n, k]
+                    e += h[k] * d * d
+                assert abs(e - r["err"][j, n, g]) <= 1e-12 * max(e, 1e-30)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -66,6 +66,16 @@ MUTATIONS = {
                                            "return n * k + 3 * n * (k // group_size)"),
     "all-zero group keeps step 0": ("        step[step == 0.0] = 1.0\n        z = np.clip",
                                     "        z = np.clip"),
+    "clip bound divides by the ratio": ("np.max(np.abs(grp), axis=2) * c)",
+                                        "np.max(np.abs(grp), axis=2) / c)"),
+    "clip bound left at the low end only": ("            hi = np.minimum(hi, bound)\n", ""),
+    "clip error not weighted by the energy": ("err[j] = (d * d * h[None, :])",
+                                              "err[j] = (d * d * h.mean())"),
+    "clip error on |d| instead of d squared": ("err[j] = (d * d * h[None, :])",
+                                               "err[j] = (np.abs(d) * h[None, :])"),
+    "energy sums |x|": ("h += X64[t] * X64[t]", "h += np.abs(X64[t])"),
+    "clip picks the last minimiser": ("best = np.argmin(err, axis=0)",
+                                      "best = len(r) - 1 - np.argmin(err[::-1], axis=0)"),
 }
 
 
