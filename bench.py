@@ -57,7 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--case", default=None,
                     help="run one kernel family on a small case and exit (for profiler "
                          "captures): 'search' (statistic, alpha search and pack of the "
-                         "workload's layer, 3 times) or 'w4a16:N:K:M' (4 launches of one shape)")
+                         "workload's layer, 3 times), 'clip' (one layer step, then the clipping search "
+                         "and clipped pack 5 times) or 'w4a16:N:K:M' (4 launches of one shape)")
     return ap.parse_args(argv)
 
 
@@ -808,6 +809,65 @@ def search_workloads(awq, torch, peaks, reps=3):
     return out
 
 
+# fp32 lane operations one clip-ratio evaluation of one weight needs at the least: the code
+# (one fma into the rounding domain, clamp low, clamp high, remove the offset), the dequantised
+# value (times the step, times 1/s), the difference, and the energy-weighted square (mul, fma)
+CLIP_OPS_PER_EVAL = 9
+
+
+def clip_timing(awq, torch, step, ratios, reps=10):
+    """Per-group clipping on the benchmark layer after its scale search: the channel energy
+    (a calib_stats launch), the ratio search and the clipped pack, timed per kernel over reps
+    passes with L2 flushed before each. The search kernel is bound by fp32 issue: its peak is
+    the SM count x 128 fp32 lanes x the SM clock, in lane operations per second."""
+    a, st = awq, step.stream
+    dev = step.W.device
+    n_r = len(ratios)
+    energy = torch.empty(step.K, dtype=torch.float32, device=dev)
+    clip = torch.empty((step.K // step.G, step.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+    def once():
+        a.awq_clip_search(step.W, step.N, step.K, step.X, step.T, step.s, ratios, n_r, step.G,
+                          False, energy, clip, st)
+        a.awq_quantize_pack_clip(step.W, step.N, step.K, step.s, clip, step.G, False, step.q,
+                                 step.sc, step.z, st)
+
+    for _ in range(3):
+        once()
+    a.awq_stream_status()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    torch.cuda.synchronize()
+    a.awq_profile_begin()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record()
+        once()
+        e1.record()
+    torch.cuda.synchronize()
+    prof = a.awq_profile_end()
+    a.awq_stream_status()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps
+    per = {k: round(v[1] * 1e3 / v[0], 3) for k, v in prof.items()}
+    evals = step.N * step.K * n_r
+    props = torch.cuda.get_device_properties(dev)
+    peak = props.multi_processor_count * 128 * 2032e6
+    us = per.get("clip_search")
+    achieved = evals * CLIP_OPS_PER_EVAL / (us * 1e-6) if us else None
+    return {
+        "layer": f"{step.N}x{step.K}, T={step.T}, G={step.G}, asymmetric, searched scale",
+        "n_ratio": n_r, "ms_per_layer": round(ms, 4), "kernels_us": per,
+        "roofline": {"bound": "alu", "kernel": "clip_search_kernel",
+                     "achieved": round(achieved / 1e12, 2) if achieved else None,
+                     "peak": round(peak / 1e12, 2), "unit": "T fp32 lane-ops/s",
+                     "frac": round(achieved / peak, 4) if achieved else None,
+                     "ops_per_eval": CLIP_OPS_PER_EVAL, "evals_per_launch": evals},
+        "timing": "energy + ratio search + clipped pack per pass, CUDA events, L2 flushed "
+                  "(256 MB write) before each pass",
+    }
+
+
 def stack_layers(torch):
     """The 224 linears of the synthetic 7B-like stack on the device (W and its calibration X;
     the down-projections take the gated input of their block's gate and up projections)."""
@@ -1115,6 +1175,8 @@ def run_ours(args):
         line["w4a16_stack_decode_g64"] = [{k: r[k] for k in ("M", "ms_per_token_step",
                                                               "tokens_per_s", "frac_hbm")}
                                           for r in sd64]
+    if rank == 0 and args.workload == WORKLOAD:
+        line["clip"] = clip_timing(awq, torch, step, synth.clip_ratios(10))
     if rank == 0 and not args.no_workloads:
         line["search_layers"] = search_workloads(awq, torch, peaks)
         stack, swl, slayers = stack_search(awq, torch, peaks)
@@ -1253,6 +1315,11 @@ def run_case(args):
         step = LayerStep(awq, torch, synth.make_layer(args.workload, 0), wl, torch.device("cuda", 0))
         for _ in range(3):
             step.enqueue()
+    elif args.case == "clip":
+        wl, _ = layer_units(args.workload)
+        step = LayerStep(awq, torch, synth.make_layer(args.workload, 0), wl, torch.device("cuda", 0))
+        step.enqueue()
+        clip_timing(awq, torch, step, synth.clip_ratios(10), reps=2)
     elif args.case.startswith("w4a16:"):
         N, K, M = (int(v) for v in args.case.split(":")[1:4])
         gen = torch.Generator(device="cuda").manual_seed(5)

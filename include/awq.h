@@ -171,6 +171,36 @@ awq_status_t awq_quantize_pack(const void* W_f16, int64_t N, int64_t K, const fl
                                uint8_t* zeros, awq_stream_t stream);
 
 /*
+ * Per-group clipping search, run after the alpha search (the pages print no clipping step, so
+ * the rule is a reading: "AWQ Math", "CPU-SLM implications and common pitfalls" only warns to
+ * watch the group size). For each group of each output row and each ratio c of `ratios`, the
+ * group's magnitudes are bounded by b = fp32(c max|w'|), w' = fp32(W s): the asymmetric range
+ * ends become min(hi, b) and max(lo, -b) (hi and lo widened to hold 0 as usual), the symmetric
+ * max|w'| becomes b, and weights beyond take the end codes. The group's error is
+ * e(c) = sum_k h_k (W - w_hat)^2 over its channels, h_k = sum_t X[t, k]^2 (the layer's output
+ * error on the calibration set with the cross-channel terms dropped), w_hat the dequantised
+ * weight (q - z) step16 / s; the first ratio with the smallest e (fp32) wins.
+ *   W_f16   [N, K] fp16;  X_f16 [T, K] fp16;  s [K] fp32 (the searched scale) or NULL (s = 1)
+ *   ratios  host [n_ratio] fp32 in (0, 1], 1 <= n_ratio <= 32 (e.g. 1 - j/20 for j < 10;
+ *           with ratios[0] = 1 a group is clipped only where that strictly lowers its error)
+ *   energy  [K] fp32 device out: h (written by the call, fixed summation order)
+ *   clip_out [K/G, N] fp32 device out: the chosen ratio of each group (indexed like scales)
+ * Two kernels on `stream`. awq_quantize_pack_clip then packs with those ratios.
+ */
+awq_status_t awq_clip_search(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
+                             int64_t T, const float* s, const float* ratios, int32_t n_ratio,
+                             awq_qcfg_t cfg, float* energy, float* clip_out, awq_stream_t stream);
+
+/*
+ * awq_quantize_pack with each group's magnitudes bounded as awq_clip_search describes:
+ *   clip [K/G, N] fp32 ratios in (0, 1] (required; all ones gives awq_quantize_pack's output).
+ * Every other argument as for awq_quantize_pack; the packed format is unchanged.
+ */
+awq_status_t awq_quantize_pack_clip(const void* W_f16, int64_t N, int64_t K, const float* s,
+                                    const float* clip, awq_qcfg_t cfg, uint32_t* qweight,
+                                    void* scales_f16, uint8_t* zeros, awq_stream_t stream);
+
+/*
  * The quantisation residual of one scale vector: the operand the search scores, one candidate
  * of "AWQ Math", "Searching the scale" (the output error of that candidate is the mean of
  * (X D^T)^2 / 2^(2p) over tokens and outputs).
@@ -303,7 +333,8 @@ typedef enum {
   AWQ_K_SCALE_ROWS = 13,  /* awq_scale_rows */
   AWQ_K_RMSNORM = 14,     /* awq_rmsnorm */
   AWQ_K_SILU_MUL = 15,    /* awq_silu_mul */
-  AWQ_K_COUNT = 16
+  AWQ_K_CLIP_SEARCH = 16, /* awq_clip_search (its channel-energy kernel counts as calib_stats) */
+  AWQ_K_COUNT = 17
 } awq_kernel_id_t;
 
 /*

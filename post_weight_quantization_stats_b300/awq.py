@@ -55,6 +55,10 @@ _SIGNATURES = {
                                          _c_void_p, _c_void_p, _c_void_p]),
     "awq_quant_residual": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, QCfg,
                                           _c_void_p, _c_void_p, _c_void_p]),
+    "awq_clip_search": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i64, _c_void_p,
+                                       _c_void_p, _i32, QCfg, _c_void_p, _c_void_p, _c_void_p]),
+    "awq_quantize_pack_clip": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, QCfg,
+                                              _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "awq_w4a16_gemm": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
                                       _c_void_p, _c_void_p, QCfg, _c_void_p, _c_void_p]),
     "awq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -72,7 +76,7 @@ _SIGNATURES = {
 
 KERNELS = ("calib_stats", "scale_grid", "absmax", "residual", "score", "finalize",
            "quantize_pack", "gemv", "gemm_tc", "gram_prep", "gram", "score_gram", "gram_search",
-           "scale_rows", "rmsnorm", "silu_mul")
+           "scale_rows", "rmsnorm", "silu_mul", "clip_search")
 SCORE_MODES = {"auto": 0, "direct": 1, "gram": 2, "gram_launches": 3}
 
 _lib = None
@@ -179,6 +183,21 @@ def awq_quantize_pack(W, N, K, s, group_size, symmetric, qweight, scales, zeros,
         _ptr(zeros), _stream(stream)))
 
 
+def awq_clip_search(W, N, K, X, T, s, ratios, n_ratio, group_size, symmetric, energy, clip_out,
+                    stream=None, bits=4):
+    arr = (ctypes.c_float * int(n_ratio))(*[float(r) for r in ratios])
+    _check("awq_clip_search", lib().awq_clip_search(
+        _ptr(W), N, K, _ptr(X), T, _ptr(s), ctypes.cast(arr, ctypes.c_void_p), n_ratio,
+        _cfg(group_size, symmetric, bits), _ptr(energy), _ptr(clip_out), _stream(stream)))
+
+
+def awq_quantize_pack_clip(W, N, K, s, clip, group_size, symmetric, qweight, scales, zeros,
+                           stream=None, bits=4):
+    _check("awq_quantize_pack_clip", lib().awq_quantize_pack_clip(
+        _ptr(W), N, K, _ptr(s), _ptr(clip), _cfg(group_size, symmetric, bits), _ptr(qweight),
+        _ptr(scales), _ptr(zeros), _stream(stream)))
+
+
 def awq_quant_residual(W, N, K, s, inv_s, group_size, symmetric, absmax_bits, D, stream=None,
                        bits=4):
     _check("awq_quant_residual", lib().awq_quant_residual(
@@ -263,6 +282,32 @@ def quantize_pack(W, s=None, group_size=128, symmetric=False, stream=None, bits=
     sc = torch.empty((K // group_size, N), dtype=torch.float16, device=W.device)
     z = torch.empty((K // group_size, N), dtype=torch.uint8, device=W.device)
     awq_quantize_pack(W, N, K, s, group_size, symmetric, q, sc, z, stream, bits)
+    return q, sc, z
+
+
+def clip_search(W, X, s=None, ratios=None, group_size=128, symmetric=False, stream=None, bits=4):
+    """(clip [K/G, N] fp32, energy [K] fp32): each group's clip ratio (awq_clip_search); ratios
+    default to 1 - j/20 for j < 10."""
+    import torch
+    N, K = W.shape
+    T = X.shape[0]
+    if ratios is None:
+        ratios = [1.0 - j / 20.0 for j in range(10)]
+    energy = torch.empty(K, dtype=torch.float32, device=W.device)
+    clip = torch.empty((K // group_size, N), dtype=torch.float32, device=W.device)
+    awq_clip_search(W, N, K, X, T, s, ratios, len(ratios), group_size, symmetric, energy, clip,
+                    stream, bits)
+    return clip, energy
+
+
+def quantize_pack_clip(W, s, clip, group_size=128, symmetric=False, stream=None, bits=4):
+    """quantize_pack with each group's magnitudes bounded by clip [K/G, N] (see awq.h)."""
+    import torch
+    N, K = W.shape
+    q = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    sc = torch.empty((K // group_size, N), dtype=torch.float16, device=W.device)
+    z = torch.empty((K // group_size, N), dtype=torch.uint8, device=W.device)
+    awq_quantize_pack_clip(W, N, K, s, clip, group_size, symmetric, q, sc, z, stream, bits)
     return q, sc, z
 
 

@@ -252,8 +252,9 @@ awq_status_t launch_k(void (*kern)(P...), dim3 grid, int threads, size_t smem, i
 
 // ------------------------------------------------------------------ launch helpers
 
+// squares = false: the statistic mean |x|; true: the channel energy sum x^2 (clipping search)
 awq_status_t launch_calib_stats(const __half* X, int64_t T, int64_t K, int64_t ldx, float* m,
-                                const DeviceInfo* d, cudaStream_t st) {
+                                const DeviceInfo* d, cudaStream_t st, bool squares = false) {
   // boxes of 128 rows x 64 columns of X (row stride ldx); columns past K and rows past T read
   // as zero
   CUtensorMap map;
@@ -261,19 +262,27 @@ awq_status_t launch_calib_stats(const __half* X, int64_t T, int64_t K, int64_t l
                          stats::BOX_ROWS));
   dim3 grid(static_cast<unsigned>((K + stats::COLS - 1) / stats::COLS), stats::CLUSTER);
   prof_start(AWQ_K_CALIB_STATS, st);
-  stats::calib_stats_kernel<<<grid, stats::THREADS, 0, st>>>(map, static_cast<int>(T),
-                                                             static_cast<int>(K), m, d->status,
-                                                             g_wait_limit_ns.load());
+  auto kern = squares ? stats::calib_stats_kernel<true> : stats::calib_stats_kernel<false>;
+  kern<<<grid, stats::THREADS, 0, st>>>(map, static_cast<int>(T), static_cast<int>(K), m,
+                                        d->status, g_wait_limit_ns.load());
   return launched(AWQ_K_CALIB_STATS, st);
+}
+
+// Grid of the run-per-thread kernels (quantize_pack_kernel, clip_search_kernel): row blocks on
+// x, one group per block on y.
+template <int MAXRUN>
+dim3 run_grid(int64_t N, int64_t K, int G) {
+  const int rows = G == 128 ? RunShape<128, MAXRUN>::ROWS
+                            : (G == 64 ? RunShape<64, MAXRUN>::ROWS : RunShape<32, MAXRUN>::ROWS);
+  return dim3(static_cast<unsigned>((N + rows - 1) / rows), static_cast<unsigned>(K / G));
 }
 
 awq_status_t launch_quantize_pack(const __half* W, int64_t N, int64_t K, const float* s,
                                   awq_qcfg_t cfg, uint32_t* q, __half* scales, uint8_t* zeros,
-                                  cudaStream_t st) {
-  QuantArgs a{W, s, q, scales, cfg.symmetric ? nullptr : zeros, static_cast<int>(N),
+                                  cudaStream_t st, const float* clip = nullptr) {
+  QuantArgs a{W, s, clip, q, scales, cfg.symmetric ? nullptr : zeros, static_cast<int>(N),
               static_cast<int>(K), cfg.symmetric, cfg_bits(cfg)};
-  const dim3 grid(static_cast<unsigned>((N + 8 * QROWS - 1) / (8 * QROWS)),
-                  static_cast<unsigned>((K / 8 + 31) / 32));
+  const dim3 grid = run_grid<PACK_RUN>(N, K, cfg.group_size);
   prof_start(AWQ_K_QUANTIZE_PACK, st);
   if (cfg.group_size == 128)
     quantize_pack_kernel<128><<<grid, 256, 0, st>>>(a);
@@ -867,6 +876,64 @@ awq_status_t awq_quantize_pack(const void* W_f16, int64_t N, int64_t K, const fl
   return launch_quantize_pack(static_cast<const __half*>(W_f16), N, K, s, cfg, qweight,
                               static_cast<__half*>(scales_f16), zeros,
                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+awq_status_t awq_quantize_pack_clip(const void* W_f16, int64_t N, int64_t K, const float* s,
+                                    const float* clip, awq_qcfg_t cfg, uint32_t* qweight,
+                                    void* scales_f16, uint8_t* zeros, awq_stream_t stream) {
+  AWQ_TRY(check_cfg(cfg));
+  if (!W_f16 || !clip || !qweight || !scales_f16 || (!cfg.symmetric && !zeros))
+    return AWQ_ERR_INVALID_ARG;
+  AWQ_TRY(check_nk(N, K, cfg));
+  if (!aligned16(W_f16) || !aligned16(qweight) || !aligned16(scales_f16) || !aligned4(clip) ||
+      (s && !aligned16(s)) || (zeros && !aligned16(zeros)))
+    return AWQ_ERR_MISALIGNED;
+  DeviceInfo* d = nullptr;
+  AWQ_TRY(device_info(&d));
+  return launch_quantize_pack(static_cast<const __half*>(W_f16), N, K, s, cfg, qweight,
+                              static_cast<__half*>(scales_f16), zeros,
+                              reinterpret_cast<cudaStream_t>(stream), clip);
+}
+
+awq_status_t awq_clip_search(const void* W_f16, int64_t N, int64_t K, const void* X_f16,
+                             int64_t T, const float* s, const float* ratios, int32_t n_ratio,
+                             awq_qcfg_t cfg, float* energy, float* clip_out,
+                             awq_stream_t stream) {
+  AWQ_TRY(check_cfg(cfg));
+  if (!W_f16 || !X_f16 || !ratios || !energy || !clip_out || T < 1) return AWQ_ERR_INVALID_ARG;
+  if (n_ratio < 1 || n_ratio > MAX_CLIP_RATIOS) return AWQ_ERR_INVALID_ARG;
+  for (int j = 0; j < n_ratio; ++j)
+    if (!(ratios[j] > 0.0f && ratios[j] <= 1.0f)) return AWQ_ERR_INVALID_ARG;
+  AWQ_TRY(check_nk(N, K, cfg));
+  if (T * K > kMaxElems) return AWQ_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(W_f16) || !aligned16(X_f16) || (s && !aligned16(s)) || !aligned16(energy) ||
+      !aligned4(clip_out))
+    return AWQ_ERR_MISALIGNED;
+  DeviceInfo* d = nullptr;
+  AWQ_TRY(device_info(&d));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the channel energy sum_t x^2 (the statistic kernel, squares instead of magnitudes)
+  AWQ_TRY(launch_calib_stats(static_cast<const __half*>(X_f16), T, K, K, energy, d, st, true));
+  ClipArgs a{};
+  a.W = static_cast<const __half*>(W_f16);
+  a.s = s;
+  a.energy = energy;
+  a.clip = clip_out;
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.symmetric = cfg.symmetric;
+  a.bits = cfg_bits(cfg);
+  a.n_ratio = n_ratio;
+  for (int j = 0; j < n_ratio; ++j) a.ratios[j] = ratios[j];
+  const dim3 grid = run_grid<CLIP_RUN>(N, K, cfg.group_size);
+  prof_start(AWQ_K_CLIP_SEARCH, st);
+  if (cfg.group_size == 128)
+    clip_search_kernel<128><<<grid, 256, 0, st>>>(a);
+  else if (cfg.group_size == 64)
+    clip_search_kernel<64><<<grid, 256, 0, st>>>(a);
+  else
+    clip_search_kernel<32><<<grid, 256, 0, st>>>(a);
+  return launched(AWQ_K_CLIP_SEARCH, st);
 }
 
 awq_status_t awq_quant_residual(const void* W_f16, int64_t N, int64_t K, const float* s,

@@ -29,16 +29,26 @@ constexpr int BOX_ROWS = 128;  // rows per TMA box
 constexpr int STAGES = 2;
 constexpr int BOX_BYTES = BOX_ROWS * COLS * 2;
 
-__device__ __forceinline__ void add_abs8(const uint4& raw, float (&acc)[8]) {
+// SQ = false: |x| (the statistic); SQ = true: x^2 (the channel energy of the clipping search).
+template <bool SQ>
+__device__ __forceinline__ void add8(const uint4& raw, float (&acc)[8]) {
   const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(__habs2(h2[i]));
-    acc[2 * i] += f.x;
-    acc[2 * i + 1] += f.y;
+    if (SQ) {
+      const float2 f = __half22float2(h2[i]);
+      acc[2 * i] = fmaf(f.x, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(f.y, f.y, acc[2 * i + 1]);
+    } else {
+      const float2 f = __half22float2(__habs2(h2[i]));
+      acc[2 * i] += f.x;
+      acc[2 * i + 1] += f.y;
+    }
   }
 }
 
+// SQ = false: m_j = (1/T) sum_t |X[t, j]|. SQ = true: m_j = sum_t X[t, j]^2 (no division).
+template <bool SQ>
 __global__ void __cluster_dims__(1, CLUSTER, 1) __launch_bounds__(THREADS)
     calib_stats_kernel(const __grid_constant__ CUtensorMap tmX, int T, int K, float* __restrict__ m,
                        int* status, unsigned long long limit_ns) {
@@ -83,7 +93,7 @@ __global__ void __cluster_dims__(1, CLUSTER, 1) __launch_bounds__(THREADS)
     if (ok) {
 #pragma unroll
       for (int r = slot; r < BOX_ROWS; r += SLOTS)
-        if (r < rows) add_abs8(*reinterpret_cast<const uint4*>(ring[s] + r * COLS * 2 + cl * 2), acc);
+        if (r < rows) add8<SQ>(*reinterpret_cast<const uint4*>(ring[s] + r * COLS * 2 + cl * 2), acc);
     }
     __syncthreads();   // every thread is done with stage s
     if (tid == 0 && j + STAGES < nbox && !abort_flag) {
@@ -111,7 +121,7 @@ __global__ void __cluster_dims__(1, CLUSTER, 1) __launch_bounds__(THREADS)
 #pragma unroll
     for (int r = 0; r < CLUSTER; ++r) sum += cluster.map_shared_rank(cta_sum, r)[tid];
     const int c = col0 + tid;
-    if (c < K) m[c] = __fdiv_rn(sum, static_cast<float>(T));
+    if (c < K) m[c] = SQ ? sum : __fdiv_rn(sum, static_cast<float>(T));
   }
   cluster.sync();
 }

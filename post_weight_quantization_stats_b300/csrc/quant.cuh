@@ -105,11 +105,10 @@ __device__ __forceinline__ float rint_quotient(float wp, const GroupParams& g) {
   return r;
 }
 
-// ------------------------------------------------------------------ quantize + pack kernel
-
 struct QuantArgs {
   const __half* W;      // [N, K]
   const float* s;       // [K] or nullptr
+  const float* clip;    // [K/G, N] clip ratios or nullptr (no clipping)
   uint32_t* qweight;    // [N, K/8]
   __half* scales;       // [K/G, N]
   uint8_t* zeros;       // [K/G, N] or nullptr
@@ -117,11 +116,12 @@ struct QuantArgs {
   int bits;             // code width: 4, 3 or 2
 };
 
-// Row-tiled launch shape shared by quantize_pack_kernel and residual_kernel: a block of 8 warps
-// covers 32 packed words (256 channels) of 8 * QROWS rows (rows along grid x, 256-channel column
-// chunks along grid y); lane l owns word 32 blockIdx.y + l of the QROWS rows of its warp. The per-channel scales are loaded once per lane and the QROWS
-// 16-byte weight loads are issued together, so every thread keeps 64 bytes of HBM reads in
-// flight. A group (G / 8 words) is G / 8 consecutive lanes of one row.
+// Row-tiled launch shape of residual_kernel (and the residual warps of the search kernels): a
+// block of 8 warps covers 32 packed words (256 channels) of 8 * QROWS rows (rows along grid x,
+// 256-channel column chunks along grid y); lane l owns word 32 blockIdx.y + l of the QROWS rows
+// of its warp. The per-channel scales are loaded once per lane and the QROWS 16-byte weight
+// loads are issued together, so every thread keeps 64 bytes of HBM reads in flight. A group
+// (G / 8 words) is G / 8 consecutive lanes of one row.
 constexpr int QROWS = 4;
 
 __device__ __forceinline__ void load8f(const float* p, bool ok, float fill, float (&v)[8]) {
@@ -146,90 +146,339 @@ __device__ __forceinline__ void unpack8(const uint4& raw, float (&w)[8]) {
   }
 }
 
+// ------------------------------------------------------------------ quantize + pack kernel
+
+// Run-per-thread launch shape of quantize_pack_kernel and clip_search_kernel: a thread owns a
+// run of RUN consecutive channels of one row (RUN <= G), so a group is G / RUN adjacent lanes
+// (TEAM). The group's min and max then take log2(TEAM) shuffles and its step and zero point are
+// computed once per thread, not once per 8 channels. A block of 256 threads covers 256 / TEAM
+// consecutive rows of one group (rows along grid x, groups along grid y); its lanes read the
+// same channels of different rows, so the per-channel loads (scales, energies) are warp-wide
+// broadcasts, and the step and zero point stores are coalesced. Both run 32 channels per thread:
+// the pack in 64 registers (four blocks per SM keep enough reads in flight), the clipping
+// search, which holds its run's w' over all ratios, at three blocks per SM (measured against
+// 64-channel runs at two).
+template <int G, int MAXRUN>
+struct RunShape {
+  static constexpr int RUN = G < MAXRUN ? G : MAXRUN;   // channels per thread
+  static constexpr int TEAM = G / RUN;                  // threads per group: 1, 2 or 4
+  static constexpr int ROWS = 256 / TEAM;               // rows per block
+  static_assert(G % RUN == 0 && TEAM <= 4, "group sizes 32, 64 and 128");
+};
+constexpr int PACK_RUN = 32;
+constexpr int CLIP_RUN = 32;
+
+// min and max over the TEAM lanes of a group (adjacent lanes; every lane takes the shuffles)
+template <int TEAM>
+__device__ __forceinline__ void team_range(float& lo, float& hi) {
+#pragma unroll
+  for (int o = TEAM / 2; o >= 1; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+}
+
+// The thread's run: its RUN / 8 16-byte weight loads issued together, then w' = fl32(w s) as
+// RUN / 2 pairs (w itself without a scale) and the run's smallest and largest w'. Rows past N
+// load zeros (their results are never stored).
+template <int RUN>
+__device__ __forceinline__ void load_run(const __half* W, const float* s, long long off, int k0,
+                                         bool ok, float2 (&v)[RUN / 2], float& lo, float& hi) {
+  uint4 raw[RUN / 8];
+#pragma unroll
+  for (int i = 0; i < RUN / 8; ++i)
+    raw[i] = ok ? __ldg(reinterpret_cast<const uint4*>(W + off) + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int i = 0; i < RUN / 8; ++i) {
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw[i]);
+    float sv[8];
+    load8f(s + k0 + 8 * i, s != nullptr, 1.0f, sv);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 w2 = __half22float2(h2[p]);
+      v[4 * i + p] = s ? mul2_rn(w2, make_float2(sv[2 * p], sv[2 * p + 1])) : w2;
+    }
+  }
+  lo = fminf(v[0].x, v[0].y);
+  hi = fmaxf(v[0].x, v[0].y);
+#pragma unroll
+  for (int p = 1; p < RUN / 2; ++p) {
+    lo = fminf(lo, fminf(v[p].x, v[p].y));
+    hi = fmaxf(hi, fmaxf(v[p].x, v[p].y));
+  }
+}
+
+// The codes in the shifted domain: with C = 1.5 * 2^23 + zero (an integer whose unit in the
+// last place is 1), u = fl32(w' rcp + C) = C + rint(w' rcp) in one FMA, exactly the integer
+// rint_quotient gives unless w' rcp - rint(w' rcp) lies within 2^-17 of +-1/2 (checked per
+// 8 channels, IEEE division there). The clamped u holds the stored code in its low four bits.
+// Element pairs go through the paired fp32 instructions (the same IEEE operations).
+constexpr float kShift = 0x1.8p23f;
+constexpr float kNearTie = 0.5f - 0x1p-17f;
+
 template <int G>
-__global__ void __launch_bounds__(256) quantize_pack_kernel(QuantArgs a) {
-  constexpr int TEAM = G / 8;
-  const int kw = a.K >> 3;                                   // words per row
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int w = blockIdx.y * 32 + lane;
-  const bool wok = w < kw;
-  const int k0 = (wok ? w : 0) * 8;
-  const int rbase = (blockIdx.x * 8 + warp) * QROWS;
-  float sv[8];
-  load8f(a.s + k0, wok && a.s != nullptr, 1.0f, sv);
-  uint4 raw[QROWS];
-#pragma unroll
-  for (int r = 0; r < QROWS; ++r) {
-    const int row = rbase + r;
-    raw[r] = (wok && row < a.N)
-                 ? __ldg(reinterpret_cast<const uint4*>(a.W + static_cast<long long>(row) * a.K + k0))
-                 : make_uint4(0, 0, 0, 0);
+__global__ void __launch_bounds__(256, 4) quantize_pack_kernel(QuantArgs a) {
+  using S = RunShape<G, PACK_RUN>;
+  constexpr int RUN = S::RUN;
+  const int t = threadIdx.x % S::TEAM;                      // run within the group
+  const int row = blockIdx.x * S::ROWS + threadIdx.x / S::TEAM;
+  const int gi = blockIdx.y;                                // group index along K
+  const int k0 = gi * G + t * RUN;
+  const bool ok = row < a.N;
+  const long long r64 = ok ? row : 0;
+  float2 v[RUN / 2];
+  float lo, hi;
+  load_run<RUN>(a.W, a.s, r64 * a.K + k0, k0, ok, v, lo, hi);
+  team_range<S::TEAM>(lo, hi);
+  if (a.clip != nullptr) {
+    // magnitudes bounded by b = fl32(c max|w'|): the range ends are cut to it
+    const float cr = a.clip[static_cast<long long>(gi) * a.N + r64];
+    const float b = __fmul_rn(fmaxf(hi, -lo), cr);
+    hi = fminf(fmaxf(hi, 0.0f), b);
+    lo = fmaxf(fminf(lo, 0.0f), -b);
   }
-  const bool sym = a.symmetric != 0;
-  // The codes in the shifted domain: with C = 1.5 * 2^23 + zero (an integer whose unit in the
-  // last place is 1), u = fl32(w' rcp + C) = C + rint(w' rcp) in one FMA, exactly the integer
-  // rint_quotient gives unless w' rcp - rint(w' rcp) lies within 2^-17 of +-1/2 (checked once
-  // per lane, IEEE division there). The clamped u holds the stored code in its low four bits.
-  // Element pairs go through the paired fp32 instructions (the same IEEE operations).
-  constexpr float kM = 0x1.8p23f;
+  const GroupParams g = group_params_of(lo, hi, a.symmetric != 0, a.bits);
+  const float c = __fadd_rn(kShift, g.zero);
+  const float2 c2 = make_float2(c, c), rcp2 = make_float2(g.rcp, g.rcp);
   const float2 m1 = make_float2(-1.0f, -1.0f);
+  const float ulo = __fadd_rn(kShift, g.clo), uhi = __fadd_rn(kShift, g.chi);
+  uint32_t words[RUN / 8];
 #pragma unroll
-  for (int r = 0; r < QROWS; ++r) {
-    const int row = rbase + r;
-    float wv[8];
-    unpack8(raw[r], wv);
-    float2 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 w2 = make_float2(wv[2 * i], wv[2 * i + 1]);
-      v[i] = a.s ? mul2_rn(w2, make_float2(sv[2 * i], sv[2 * i + 1])) : w2;
-    }
-    float lo = fminf(v[0].x, v[0].y), hi = fmaxf(v[0].x, v[0].y);
-#pragma unroll
-    for (int i = 1; i < 4; ++i) {
-      lo = fminf(lo, fminf(v[i].x, v[i].y));
-      hi = fmaxf(hi, fmaxf(v[i].x, v[i].y));
-    }
-#pragma unroll
-    for (int o = TEAM / 2; o >= 1; o >>= 1) {   // every lane shuffles
-      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    const GroupParams g = group_params_of(lo, hi, sym, a.bits);
-    const float c = __fadd_rn(kM, g.zero);
-    const float2 c2 = make_float2(c, c), rcp2 = make_float2(g.rcp, g.rcp);
-    float fmax_abs = 0.0f;
+  for (int i = 0; i < RUN / 8; ++i) {
     float2 u[4];
+    float fm = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      u[i] = fma2_rn(v[i], rcp2, c2);
-      const float2 f = fma2_rn(v[i], rcp2, fma2_rn(u[i], m1, c2));
-      fmax_abs = fmaxf(fmax_abs, fmaxf(fabsf(f.x), fabsf(f.y)));
+    for (int p = 0; p < 4; ++p) {
+      u[p] = fma2_rn(v[4 * i + p], rcp2, c2);
+      const float2 f = fma2_rn(v[4 * i + p], rcp2, fma2_rn(u[p], m1, c2));
+      fm = fmaxf(fm, fmaxf(fabsf(f.x), fabsf(f.y)));
     }
-    if (fmax_abs >= 0.5f - 0x1p-17f) {   // see rint_quotient
+    if (fm >= kNearTie) {   // see rint_quotient
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        u[i].x = __fadd_rn(rintf(__fdiv_rn(v[i].x, g.step)), c);
-        u[i].y = __fadd_rn(rintf(__fdiv_rn(v[i].y, g.step)), c);
+      for (int p = 0; p < 4; ++p) {
+        u[p].x = __fadd_rn(rintf(__fdiv_rn(v[4 * i + p].x, g.step)), c);
+        u[p].y = __fadd_rn(rintf(__fdiv_rn(v[4 * i + p].y, g.step)), c);
       }
     }
-    const float ulo = __fadd_rn(kM, g.clo), uhi = __fadd_rn(kM, g.chi);
-    if (wok && row < a.N) {
-      uint32_t packed = 0;
+    uint32_t packed = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t c0 = __float_as_uint(fminf(fmaxf(u[i].x, ulo), uhi)) & 0xFu;
-        const uint32_t c1 = __float_as_uint(fminf(fmaxf(u[i].y, ulo), uhi)) & 0xFu;
-        packed |= (c0 | (c1 << 4)) << (8 * i);
-      }
-      a.qweight[static_cast<long long>(row) * kw + w] = packed;
-      if ((lane & (TEAM - 1)) == 0) {
-        const long long gi = static_cast<long long>(k0 / G) * a.N + row;
-        a.scales[gi] = __float2half_rn(g.step);
-        if (!sym && a.zeros) a.zeros[gi] = static_cast<uint8_t>(g.zero);
-      }
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t c0 = __float_as_uint(fminf(fmaxf(u[p].x, ulo), uhi)) & 0xFu;
+      const uint32_t c1 = __float_as_uint(fminf(fmaxf(u[p].y, ulo), uhi)) & 0xFu;
+      packed |= (c0 | (c1 << 4)) << (8 * p);
+    }
+    words[i] = packed;
+  }
+  if (ok) {
+    uint4* dst = reinterpret_cast<uint4*>(a.qweight + r64 * (a.K >> 3) + (k0 >> 3));
+#pragma unroll
+    for (int i = 0; i < RUN / 32; ++i)
+      dst[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+    static_assert(RUN % 32 == 0, "a run packs into whole 16-byte stores");
+    if (t == 0) {
+      const long long gidx = static_cast<long long>(gi) * a.N + row;
+      a.scales[gidx] = __float2half_rn(g.step);
+      if (a.symmetric == 0 && a.zeros) a.zeros[gidx] = static_cast<uint8_t>(g.zero);
     }
   }
+}
+
+// ------------------------------------------------------------------ clipping search
+
+// Per-group clip ratio (a reading; the pages print no clipping step): for each ratio c of the
+// grid, the group's magnitudes are bounded by b = fl32(c max|w'|) (asymmetric ends cut to
+// min(hi, b) and max(lo, -b), symmetric max|w'| -> b), the group is quantised exactly as the
+// pack kernel does with that bound, and its error e(c) = sum_k h_k (W - w_hat)^2 (h the channel
+// energy sum_t x_tk^2, w_hat = (q - z) step16 / s) is accumulated in fp32 in the scaled domain:
+// W - w_hat = (w' - (q - z) step16) / s, so each term is g_k r_k^2 with g_k = fl32(h_k / fl32(s_k^2))
+// and r_k = fl32(w' - (q - z) step16) in one FMA ((q - z) step16 is exact: a small integer times
+// an fp16 value). Against the exact terms, r_k / s_k is within 2^-23 (|W| + |w_hat|) of
+// W - w_hat and g_k within 2^-23 relative of h_k / s_k^2; a thread adds its run in four fixed
+// chains (pair index mod 4), the lanes of a group their sums in a butterfly. The first ratio with the smallest error wins; the
+// group's first thread writes it to clip[g, n].
+constexpr int MAX_CLIP_RATIOS = 32;
+
+struct ClipArgs {
+  const __half* W;       // [N, K]
+  const float* s;        // [K] or nullptr
+  const float* energy;   // [K] sum_t x^2
+  float* clip;           // [K/G, N] out
+  int N, K, symmetric, bits, n_ratio;
+  float ratios[MAX_CLIP_RATIOS];
+};
+
+// 16-byte shared-memory load kept inside its loop (volatile): the channel weights are read
+// again for every ratio instead of being held in 64 registers beside the run's w'.
+__device__ __forceinline__ float4 lds_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+  return v;
+}
+
+// 16-byte read-only global loads the compiler may not merge with earlier loads of the same
+// address (volatile): the near-tie path reloads its run instead of keeping the first loads live.
+__device__ __forceinline__ uint4 ldg_u4_again(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(reinterpret_cast<uint64_t>(p)));
+  return v;
+}
+__device__ __forceinline__ float4 ldg_f4_again(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(reinterpret_cast<uint64_t>(p)));
+  return v;
+}
+
+// One pair's term of the clipping criterion: g (w' - (code - zero) step16)^2 added to acc, with
+// -(code - zero) = nq clamped to [nlo, nhi].
+__device__ __forceinline__ void clip_term(float2 vp, float2 nq, float nlo, float nhi, float2 st2,
+                                          float2 gp, float2& acc) {
+  const float2 nc = make_float2(fminf(fmaxf(nq.x, nlo), nhi), fminf(fmaxf(nq.y, nlo), nhi));
+  const float2 r = fma2_rn(nc, st2, vp);           // w' - (code - zero) step16
+  acc = fma2_rn(mul2_rn(gp, r), r, acc);
+}
+
+// The quantiser of one clip ratio in the form the criterion uses: the IEEE step (for the
+// near-tie division), its reciprocal, C = 1.5 * 2^23 + zero, the clamp range of -(code - zero)
+// and the stored fp16 step.
+struct RatioParams {
+  float step, rcp, c, nlo, nhi, st16;
+};
+
+__device__ __forceinline__ RatioParams ratio_params(float lo, float hi, float amax, float ratio,
+                                                    bool sym, int bits) {
+  const float b = __fmul_rn(amax, ratio);
+  const GroupParams g = group_params_of(fmaxf(fminf(lo, 0.0f), -b), fminf(fmaxf(hi, 0.0f), b),
+                                        sym, bits);
+  RatioParams r;
+  r.step = g.step;
+  r.rcp = g.rcp;
+  r.c = __fadd_rn(kShift, g.zero);
+  r.nlo = __fsub_rn(g.zero, g.chi);   // -(code - zero) lies in [zero - chi, zero - clo]
+  r.nhi = __fsub_rn(g.zero, g.clo);
+  r.st16 = __half2float(__float2half_rn(g.step));
+  return r;
+}
+
+template <int G>
+__global__ void __launch_bounds__(256, 3) clip_search_kernel(ClipArgs a) {
+  using S = RunShape<G, CLIP_RUN>;
+  constexpr int RUN = S::RUN;
+  constexpr int GP = RUN + 4;   // run stride in shared memory: a group's runs start on other banks
+  __shared__ __align__(16) float gsh[S::TEAM * GP];
+  const int gi = blockIdx.y;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) {
+    const int k = gi * G + i;
+    float gk = a.energy[k];
+    if (a.s) {
+      const float sk = a.s[k];
+      gk = __fdiv_rn(gk, __fmul_rn(sk, sk));
+    }
+    gsh[(i / RUN) * GP + i % RUN] = gk;
+  }
+  __syncthreads();
+  const int t = threadIdx.x % S::TEAM;
+  const int row = blockIdx.x * S::ROWS + threadIdx.x / S::TEAM;
+  const int k0 = gi * G + t * RUN;
+  const bool ok = row < a.N;
+  const long long off = (ok ? row : 0) * static_cast<long long>(a.K) + k0;
+  float2 v[RUN / 2];
+  float lo, hi;
+  load_run<RUN>(a.W, a.s, off, k0, ok, v, lo, hi);
+  team_range<S::TEAM>(lo, hi);
+  const float* gt = gsh + t * GP;
+  const bool sym = a.symmetric != 0;
+  const float amax = fmaxf(hi, -lo);
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+  float best_e = 0.0f;
+  int best_j = 0;
+#pragma unroll 1
+  for (int j = 0; j < a.n_ratio; ++j) {
+    const RatioParams P = ratio_params(lo, hi, amax, a.ratios[j], sym, a.bits);
+    const float2 c2 = make_float2(P.c, P.c), rcp2 = make_float2(P.rcp, P.rcp);
+    const float2 st2 = make_float2(P.st16, P.st16);
+    // four independent chains (pair index mod 4) for the sums and the near-tie test. The test
+    // takes the remainder g = w' rcp + nc against the clamped code: the IEEE rounding can give
+    // another clamped code only where the fast one lies within 2^-17 of a rounding boundary
+    // (|f| >= 1/2 - 2^-17 for f = w' rcp + nq, see rint_quotient) and the other candidate
+    // clamps differently, and then |g| is within 2^-17 of 1/2 (g = f inside the range, f -+ 1
+    // where the fast code is one past an end). Clamped weights far outside the range, such as
+    // a group's largest magnitude under ratio 0.6 (exactly 12.5 steps), do not trigger it.
+    // |g^2 - 1/4| <= 2^-16 covers |g| - 1/2 within 2^-17.
+    float2 e[4];
+    float fm[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      e[c] = make_float2(0.0f, 0.0f);
+      fm[c] = 1.0f;
+    }
+    const float2 mq2 = make_float2(-0.25f, -0.25f);
+#pragma unroll
+    for (int q = 0; q < RUN / 4; ++q) {
+      const float4 gq = lds_f4(gt + 4 * q);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = (2 * q + h) & 3;
+        const float2 vp = v[2 * q + h];
+        const float2 u = fma2_rn(vp, rcp2, c2);          // C + rint(w' rcp)
+        const float2 nq = fma2_rn(u, m1, c2);            // -rint(w' rcp), exact
+        const float2 nc = make_float2(fminf(fmaxf(nq.x, P.nlo), P.nhi),
+                                      fminf(fmaxf(nq.y, P.nlo), P.nhi));
+        const float2 g = fma2_rn(vp, rcp2, nc);          // remainder against the clamped code
+        const float2 tq = fma2_rn(g, g, mq2);            // g^2 - 1/4
+        fm[c] = fminf(fm[c], fminf(fabsf(tq.x), fabsf(tq.y)));
+        const float2 r = fma2_rn(nc, st2, vp);           // w' - (code - zero) step16
+        const float2 gp = h ? make_float2(gq.z, gq.w) : make_float2(gq.x, gq.y);
+        e[c] = fma2_rn(mul2_rn(gp, r), r, e[c]);
+      }
+    }
+    if (fminf(fminf(fm[0], fm[1]), fminf(fm[2], fm[3])) <= 0x1p-16f) {
+      // a near-tie in the run (rare): the same sum with IEEE division at the near-ties, the
+      // run's w' rebuilt from memory 8 channels at a time (the same products)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) e[c] = make_float2(0.0f, 0.0f);
+#pragma unroll 1
+      for (int i = 0; i < RUN / 8; ++i) {
+        const uint4 raw = ok ? ldg_u4_again(a.W + off + 8 * i) : make_uint4(0, 0, 0, 0);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+        float sv[8] = {1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f, 1.0f};
+        if (a.s) {
+          const float4 s0 = ldg_f4_again(a.s + k0 + 8 * i), s1 = ldg_f4_again(a.s + k0 + 8 * i + 4);
+          sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
+          sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+        }
+        const float4 ga = lds_f4(gt + 8 * i), gb = lds_f4(gt + 8 * i + 4);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 w2 = __half22float2(h2[p]);
+          const float2 vp = a.s ? mul2_rn(w2, make_float2(sv[2 * p], sv[2 * p + 1])) : w2;
+          float2 nq = fma2_rn(fma2_rn(vp, rcp2, c2), m1, c2);
+          const float2 f = fma2_rn(vp, rcp2, nq);
+          if (fabsf(f.x) >= kNearTie) nq.x = -rintf(__fdiv_rn(vp.x, P.step));
+          if (fabsf(f.y) >= kNearTie) nq.y = -rintf(__fdiv_rn(vp.y, P.step));
+          const float4 gg = p < 2 ? ga : gb;
+          clip_term(vp, nq, P.nlo, P.nhi, st2,
+                    (p & 1) ? make_float2(gg.z, gg.w) : make_float2(gg.x, gg.y), e[p]);
+        }
+      }
+    }
+    float err = __fadd_rn(__fadd_rn(__fadd_rn(e[0].x, e[0].y), __fadd_rn(e[1].x, e[1].y)),
+                          __fadd_rn(__fadd_rn(e[2].x, e[2].y), __fadd_rn(e[3].x, e[3].y)));
+    // the team's lanes add the same two values (in either order: the same sum in every lane)
+#pragma unroll
+    for (int o = S::TEAM / 2; o >= 1; o >>= 1)
+      err = __fadd_rn(err, __shfl_xor_sync(0xffffffffu, err, o));
+    if (j == 0 || err < best_e) {
+      best_e = err;
+      best_j = j;
+    }
+  }
+  if (ok && t == 0) a.clip[static_cast<long long>(gi) * a.N + row] = a.ratios[best_j];
 }
 
 // ------------------------------------------------------------------ search-side kernels

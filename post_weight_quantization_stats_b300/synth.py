@@ -208,6 +208,11 @@ def alpha_grid(n_alpha: int = 20) -> np.ndarray:
     return (np.arange(n_alpha, dtype=np.float64) / n_alpha).astype(np.float32)
 
 
+def clip_ratios(n_ratio: int = 10) -> np.ndarray:
+    """The clipping grid c_j = 1 - j/20, j = 0..n_ratio-1, as fp32 (1 keeps the full range)."""
+    return (1.0 - np.arange(n_ratio, dtype=np.float64) / 20.0).astype(np.float32)
+
+
 def stack_bytes(workload: str = "llama7b-stack", group_size: int = 128) -> int:
     """Packed bytes (codes + fp16 scale + uint8 zero) of every layer of a workload."""
     wl = WORKLOADS[workload]

@@ -200,3 +200,36 @@ def test_static_search_checks_arguments_before_its_size(L):
     if not torch.cuda.is_available():
         assert L.awq_search_scale_static(A, 16, 256, A, 8, None, ap, 2, cfg, A, A, None, None,
                                          None) == S["AWQ_ERR_NO_DEVICE"]
+
+
+def test_clip_calls_reject_bad_arguments_on_the_host(L):
+    """awq_clip_search and awq_quantize_pack_clip: ratio counts and values, NULL outputs, sizes
+    and alignment are checked before any CUDA call."""
+    cfg = awq.QCfg(128, 0)
+    A = 1 << 20
+    S = awq.STATUS_CODE
+
+    def ratios(*v):
+        arr = (ctypes.c_float * len(v))(*v)
+        return ctypes.cast(arr, ctypes.c_void_p), arr
+
+    good, keep1 = ratios(1.0, 0.9)
+    zero, keep2 = ratios(1.0, 0.0)
+    big, keep3 = ratios(1.0, 1.5)
+    call = L.awq_clip_search
+    assert call(A, 16, 256, A, 8, None, good, 0, cfg, A, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert call(A, 16, 256, A, 8, None, good, 33, cfg, A, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert call(A, 16, 256, A, 8, None, zero, 2, cfg, A, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert call(A, 16, 256, A, 8, None, big, 2, cfg, A, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert call(A, 16, 256, A, 8, None, good, 2, cfg, None, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert call(A, 16, 256, A, 8, None, good, 2, cfg, A, None, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert call(A, 16, 100, A, 8, None, good, 2, cfg, A, A, None) == S["AWQ_ERR_UNSUPPORTED_SHAPE"]
+    assert call(A, 16, 256, A + 2, 8, None, good, 2, cfg, A, A, None) == S["AWQ_ERR_MISALIGNED"]
+    assert call(A, 16, 256, A, 8, None, good, 2, cfg, A + 4, A, None) == S["AWQ_ERR_MISALIGNED"]
+    pack = L.awq_quantize_pack_clip
+    assert pack(A, 16, 256, None, None, cfg, A, A, A, None) == S["AWQ_ERR_INVALID_ARG"]
+    assert pack(A, 16, 256, None, A + 2, cfg, A, A, A, None) == S["AWQ_ERR_MISALIGNED"]
+    import torch
+    if not torch.cuda.is_available():
+        assert call(A, 16, 256, A, 8, None, good, 2, cfg, A, A, None) == S["AWQ_ERR_NO_DEVICE"]
+        assert pack(A, 16, 256, None, A, cfg, A, A, A, None) == S["AWQ_ERR_NO_DEVICE"]
