@@ -614,15 +614,30 @@ def w4a16_sweep(awq, torch, shapes, ms, G, peaks):
     return out
 
 
-def stack_decode(awq, torch, peaks, G=128, ms=(1,), reps=5):
-    """Decode steps (M tokens) through all 224 linears of the synthetic 7B stack, each captured
-    in one CUDA graph: weight bytes streamed per step against the HBM peak, one entry per M.
-    The packed weights are drawn once (3.4 GB at G = 128, more than L2 many times over)."""
+def stack_shapes(fuse_shared_input=False):
+    """(N, K) of each launch of one decode step through the 7B stack: its 224 linears, or with
+    the linears that read the same input concatenated along N (q/k/v as one 12288 x 4096
+    matrix, gate/up as one 22016 x 4096), as serving stacks store them: 128 launches over the
+    same weights."""
     wl = synth.WORKLOADS["llama7b-stack"]
+    if not fuse_shared_input:
+        return [(spec.n, spec.k) for spec in wl.layers]
+    out = []
+    for i in range(0, len(wl.layers), 7):
+        q, k, v, o, gate, up, down = wl.layers[i:i + 7]
+        out += [(q.n + k.n + v.n, q.k), (o.n, o.k), (gate.n + up.n, gate.k), (down.n, down.k)]
+    return out
+
+
+def stack_decode(awq, torch, peaks, G=128, ms=(1,), reps=5, fuse_shared_input=False):
+    """Decode steps (M tokens) through all 224 linears of the synthetic 7B stack (see
+    stack_shapes), each step captured in one CUDA graph: weight bytes streamed per step against
+    the HBM peak, one entry per M. The packed weights are drawn once (3.4 GB at G = 128, more
+    than L2 many times over)."""
+    shapes = stack_shapes(fuse_shared_input)
     gen = torch.Generator(device="cuda").manual_seed(11)
     weights = []
-    for spec in wl.layers:
-        N, K = spec.n, spec.k
+    for N, K in shapes:
         weights.append((N, K,
                         torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), dtype=torch.int32,
                                       device="cuda", generator=gen),
@@ -658,7 +673,7 @@ def stack_decode(awq, torch, peaks, G=128, ms=(1,), reps=5):
         awq.awq_stream_status()
         t_ms = e0.elapsed_time(e1) / reps
         gbs = total / (t_ms * 1e-3) / 1e9
-        out.append({"linears": len(wl.layers), "M": M, "group_size": G,
+        out.append({"linears": 224, "launches": len(shapes), "M": M, "group_size": G,
                     "ms_per_token_step": round(t_ms, 4),
                     "tokens_per_s": round(M / (t_ms * 1e-3), 1), "bytes_per_step": total,
                     "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
@@ -1171,6 +1186,11 @@ def run_ours(args):
         line["w4a16_stack_decode_sweep"] = [{k: r[k] for k in ("M", "ms_per_token_step",
                                                                 "tokens_per_s", "frac_hbm")}
                                             for r in sd]
+        sdf = stack_decode(awq, torch, peaks, G=128, ms=(1, 2, 4, 8, 16, 64), reps=3,
+                           fuse_shared_input=True)
+        line["w4a16_stack_decode_fused"] = [
+            {k: r[k] for k in ("M", "launches", "ms_per_token_step", "tokens_per_s", "frac_hbm")}
+            for r in sdf]
         sd64 = stack_decode(awq, torch, peaks, G=64, ms=(1, 8, 64), reps=3)
         line["w4a16_stack_decode_g64"] = [{k: r[k] for k in ("M", "ms_per_token_step",
                                                               "tokens_per_s", "frac_hbm")}

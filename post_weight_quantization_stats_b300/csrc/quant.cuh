@@ -483,13 +483,14 @@ __global__ void __launch_bounds__(256, 3) clip_search_kernel(ClipArgs a) {
 
 // ------------------------------------------------------------------ search-side kernels
 
-// s[i, k] = fp32(max(m_k, 1e-6)^alpha_i) computed in fp64 as 2^(alpha_i log2(base)), the
-// logarithm once per channel; inv_s = 1 / s (IEEE fp32). For base in [1e-6, 2^64], |log2| <= 64,
-// so the fp64 logarithm (1 ulp) and the product with alpha (half an ulp) put the exponent
-// within about 1.5 * 2^-46 of exact, and the power within about 2^-46 relative of
-// max(m, 1e-6)^alpha before its rounding to fp32 (whose spacing is 2^-23): the fp32 scale
-// equals the correctly rounded power except when the power lies that close to a rounding
-// boundary, where it is one fp32 spacing off.
+// s[i, k] = max(m_k, 1e-6)^alpha_i in fp32, inv_s = 1 / s (IEEE fp32). The logarithm
+// L = log2(base) is taken once per channel in fp64 and y = alpha_i L in fp64 (for base in
+// [1e-6, 2^64], |L| <= 64, so y is within about 2^-46 of exact); y splits into an integer n =
+// rint(y) and f = fl32(y - n) with |f| <= 1/2 (y - n is exact in fp64, its rounding to fp32 at
+// most 2^-25), and s = 2^n exp2f(f), the scaling by 2^n exact. exp2f is within 2 ulp (CUDA's
+// documented bound) and f's rounding moves the power by at most 2^-25 ln 2 relative, so s lies
+// within 3 fp32 spacings of the exact power: below 4e-7 relative. Only the logarithm and one
+// product per alpha run in fp64, whose rate on this part is a small fraction of fp32's.
 struct GridArgs {
   const float* m;  // [K]
   float* s;        // [n_alpha, K]
@@ -509,7 +510,9 @@ __global__ void __launch_bounds__(128) scale_grid_kernel(GridArgs a) {
   for (int j = 0; j < GRID_ALPHAS; ++j) {
     const int i = i0 + j;
     if (i < a.n_alpha) {
-      const float s = static_cast<float>(exp2(lb * static_cast<double>(a.alphas[i])));
+      const double y = lb * static_cast<double>(a.alphas[i]);
+      const double n = rint(y);
+      const float s = ldexpf(exp2f(static_cast<float>(y - n)), static_cast<int>(n));
       const long long idx = static_cast<long long>(i) * a.K + k;
       a.s[idx] = s;
       a.inv_s[idx] = __fdiv_rn(1.0f, s);
@@ -606,7 +609,7 @@ __device__ __forceinline__ void residual_load(const ResidualArgs& a, int rb, int
 // branch instead of one per weight, redone with IEEE division for the lane's RB rows, which
 // gives the same integers everywhere else); then the codes, w_hat and the residual. RB is
 // bounded by the registers the calling kernel can spare.
-constexpr int RES_RB = 1;
+constexpr int RES_RB = 2;
 
 template <int TEAM, int RB>
 __device__ __forceinline__ void residual_rows(const ResidualArgs& a, const ResidualRegs& r, int q0,
