@@ -136,3 +136,24 @@ def test_clip_search_full_size_sampled_rows():
     # each sampled group's criterion at its ratio is never above its unclipped one
     e_at = np.take_along_axis(r["err"], gi[None], axis=0)[0]
     assert np.all(e_at <= r["err"][0] * (1 + 1e-5))
+
+
+CLIP_WORKLOAD_LAYERS = [("llama7b-mlp", 0), ("llama7b-mlp", 2), ("llama70b-mlp", 0),
+                        ("llama70b-mlp", 1)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wl,i", CLIP_WORKLOAD_LAYERS)
+def test_clip_search_workload_sampled_rows(wl, i):
+    """The MLP workloads' layers at full size (K up to 28672, T = 8192 and 4096, the gated input
+    of the down-projections), one launch over all rows with the scale of alpha = 0.5 from the
+    GPU's statistic: ratios, energies and clipped packs of 64 sampled rows against the
+    oracle."""
+    d = synth.make_layer(wl, i)
+    X = dev(d["X"])
+    m = host(awq.calib_stats(X))
+    s = ref.fl32(ref.scale_grid(m, [0.5]))[0].astype(np.float32)
+    N = d["W"].shape[0]
+    rows = np.sort(np.random.Generator(np.random.PCG64(N + i)).choice(N, 64, replace=False))
+    del X
+    _check_clip(d["W"], d["X"], s, 128, False, 4, rows=rows)
