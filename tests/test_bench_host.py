@@ -106,3 +106,27 @@ def test_profiled_traffic_follows_every_kernel_source(tmp_path, monkeypatch):
     (csrc / "b.cuh").write_text("helpers b, changed\n")
     assert bench.profiled_traffic("k.md", ("a.cuh", "b.cuh")) is None
     assert bench.profiled_traffic("k.md", ("a.cuh", "missing.cuh")) is None
+
+
+def test_stack_shapes_fused_keeps_the_weights():
+    """The fused decode step concatenates q/k/v and gate/up along N: 4 launches per block
+    instead of 7, over exactly the same weight elements, with each fused matrix reading one
+    input (the same K)."""
+    plain = bench.stack_shapes()
+    fused = bench.stack_shapes(fuse_shared_input=True)
+    assert len(plain) == 224 and len(fused) == 128
+    assert sum(n * k for n, k in plain) == sum(n * k for n, k in fused)
+    for b in range(32):
+        q, k, v, o, gate, up, down = plain[7 * b:7 * b + 7]
+        qkv, o2, gate_up, down2 = fused[4 * b:4 * b + 4]
+        assert qkv == (q[0] + k[0] + v[0], q[1]) and q[1] == k[1] == v[1]
+        assert gate_up == (gate[0] + up[0], gate[1]) and gate[1] == up[1]
+        assert o2 == o and down2 == down
+
+
+def test_clip_ratio_grid_matches_the_oracle():
+    """The benchmark's clipping grid is the oracle's (1, 0.95, ..., 0.55)."""
+    from oracle import awq_ref as ref
+    from post_weight_quantization_stats_b300 import synth
+    assert np.array_equal(synth.clip_ratios(10), ref.clip_ratio_grid(10))
+    assert synth.clip_ratios(10)[0] == 1.0 and np.all(np.diff(synth.clip_ratios(10)) < 0)
