@@ -98,7 +98,8 @@ def _check_clip(W16, X16, s, G, sym, bits, rows=None):
 
 CLIP_CASES = [(300, 1152, 200, 128, False, 4), (256, 512, 64, 64, True, 4),
               (1, 128, 8, 128, False, 4), (130, 256, 100, 32, False, 4),
-              (200, 1024, 150, 128, False, 3), (64, 512, 96, 64, True, 3)]
+              (200, 1024, 150, 128, False, 3), (64, 512, 96, 64, True, 3),
+              (96, 256, 40, 32, True, 2), (160, 384, 50, 64, False, 2)]
 
 
 @pytest.mark.parametrize("N,K,T,G,sym,bits", CLIP_CASES)
