@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(256, 4) quantize_pack_kernel(QuantArgs a) {
 // W - w_hat = (w' - (q - z) step16) / s, so each term is g_k r_k^2 with g_k = fl32(h_k / fl32(s_k^2))
 // and r_k = fl32(w' - (q - z) step16) in one FMA ((q - z) step16 is exact: a small integer times
 // an fp16 value). Against the exact terms, r_k / s_k is within 2^-23 (|W| + |w_hat|) of
-// W - w_hat and g_k within 2^-23 relative of h_k / s_k^2; a thread adds its run in four fixed
-// chains (pair index mod 4), the lanes of a group their sums in a butterfly. The first ratio with the smallest error wins; the
+// W - w_hat and g_k within 2^-23 relative of h_k / s_k^2; a thread adds its run in two fixed
+// chains of pairs (pair index mod 2), the lanes of a group their sums in a butterfly. The first ratio with the smallest error wins; the
 // group's first thread writes it to clip[g, n].
 constexpr int MAX_CLIP_RATIOS = 32;
 
@@ -402,7 +402,8 @@ __global__ void __launch_bounds__(256, 3) clip_search_kernel(ClipArgs a) {
     const RatioParams P = ratio_params(lo, hi, amax, a.ratios[j], sym, a.bits);
     const float2 c2 = make_float2(P.c, P.c), rcp2 = make_float2(P.rcp, P.rcp);
     const float2 st2 = make_float2(P.st16, P.st16);
-    // four independent chains (pair index mod 4) for the sums and the near-tie test. The test
+    // two independent chains of pairs (pair index mod 2) for the sums and the near-tie test
+    // (four chains cost spills at three blocks per SM and measured 2.6 % slower). The test
     // takes the remainder g = w' rcp + nc against the clamped code: the IEEE rounding can give
     // another clamped code only where the fast one lies within 2^-17 of a rounding boundary
     // (|f| >= 1/2 - 2^-17 for f = w' rcp + nq, see rint_quotient) and the other candidate
@@ -410,10 +411,10 @@ __global__ void __launch_bounds__(256, 3) clip_search_kernel(ClipArgs a) {
     // where the fast code is one past an end). Clamped weights far outside the range, such as
     // a group's largest magnitude under ratio 0.6 (exactly 12.5 steps), do not trigger it.
     // |g^2 - 1/4| <= 2^-16 covers |g| - 1/2 within 2^-17.
-    float2 e[4];
-    float fm[4];
+    float2 e[2];
+    float fm[2];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       e[c] = make_float2(0.0f, 0.0f);
       fm[c] = 1.0f;
     }
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(256, 3) clip_search_kernel(ClipArgs a) {
       const float4 gq = lds_f4(gt + 4 * q);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int c = (2 * q + h) & 3;
+        const int c = h;
         const float2 vp = v[2 * q + h];
         const float2 u = fma2_rn(vp, rcp2, c2);          // C + rint(w' rcp)
         const float2 nq = fma2_rn(u, m1, c2);            // -rint(w' rcp), exact
@@ -437,11 +438,11 @@ __global__ void __launch_bounds__(256, 3) clip_search_kernel(ClipArgs a) {
         e[c] = fma2_rn(mul2_rn(gp, r), r, e[c]);
       }
     }
-    if (fminf(fminf(fm[0], fm[1]), fminf(fm[2], fm[3])) <= 0x1p-16f) {
+    if (fminf(fm[0], fm[1]) <= 0x1p-16f) {
       // a near-tie in the run (rare): the same sum with IEEE division at the near-ties, the
       // run's w' rebuilt from memory 8 channels at a time (the same products)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) e[c] = make_float2(0.0f, 0.0f);
+      for (int c = 0; c < 2; ++c) e[c] = make_float2(0.0f, 0.0f);
 #pragma unroll 1
       for (int i = 0; i < RUN / 8; ++i) {
         const uint4 raw = ok ? ldg_u4_again(a.W + off + 8 * i) : make_uint4(0, 0, 0, 0);
@@ -463,12 +464,11 @@ __global__ void __launch_bounds__(256, 3) clip_search_kernel(ClipArgs a) {
           if (fabsf(f.y) >= kNearTie) nq.y = -rintf(__fdiv_rn(vp.y, P.step));
           const float4 gg = p < 2 ? ga : gb;
           clip_term(vp, nq, P.nlo, P.nhi, st2,
-                    (p & 1) ? make_float2(gg.z, gg.w) : make_float2(gg.x, gg.y), e[p]);
+                    (p & 1) ? make_float2(gg.z, gg.w) : make_float2(gg.x, gg.y), e[p & 1]);
         }
       }
     }
-    float err = __fadd_rn(__fadd_rn(__fadd_rn(e[0].x, e[0].y), __fadd_rn(e[1].x, e[1].y)),
-                          __fadd_rn(__fadd_rn(e[2].x, e[2].y), __fadd_rn(e[3].x, e[3].y)));
+    float err = __fadd_rn(__fadd_rn(e[0].x, e[0].y), __fadd_rn(e[1].x, e[1].y));
     // the team's lanes add the same two values (in either order: the same sum in every lane)
 #pragma unroll
     for (int o = S::TEAM / 2; o >= 1; o >>= 1)
