@@ -208,3 +208,45 @@ def test_residual_shifted_domain_codes_equal_the_quotient_rule():
     # the near-boundary branch was exercised, and the samples reach quotients where the fast
     # path alone would pick the wrong integer
     assert n_edge > 0 and n_fast_wrong > 0
+
+
+def _clamp(v, lo, hi):
+    return max(lo, min(hi, v))
+
+
+@pytest.mark.parametrize("bits,symmetric", [(4, False), (4, True), (3, False), (2, True)])
+def test_clip_near_tie_test_on_the_clamped_code(bits, symmetric):
+    """The clipping search decides its codes with the fast rounding nq = -rint(w' rcp) and falls
+    back to IEEE division only where min |g^2 - 1/4| <= 2^-16, g = w' rcp + clamp(nq): the
+    remainder against the CLAMPED code. The rounding rule (rint_quotient) leaves the fast integer
+    and the IEEE one different only where the fast remainder f = w' rcp + nq has |f| >= 1/2 -
+    2^-17, and then by one step toward f's side. Checked here in exact rationals, over every
+    clamp range the quantisers use, codes up to four steps past either end and remainders
+    across [-1/2, 1/2] concentrated at both ends: wherever the other rounding would give a
+    different CLAMPED code the test fires, and it never fires for weights two or more steps
+    beyond the range (such as a group's largest magnitude under ratio 0.6, exactly 12.5 steps
+    out, which the unclamped test would send down the slow path)."""
+    half = 2 ** (bits - 1)
+    if symmetric:   # code - zero in [-2^(N-1), 2^(N-1) - 1]: -(code - zero) in [1 - half, half]
+        ranges = [(1 - half, half)]
+    else:           # codes 0 .. 2^N - 1, zero point z in that range
+        qmax = 2 ** bits - 1
+        ranges = [(z - qmax, z) for z in range(qmax + 1)]
+    eps = Fraction(1, 2 ** 17)
+    fs = [Fraction(1, 2) - eps * k / 4 for k in range(0, 9)] + [Fraction(1, 4), Fraction(0)]
+    fs = fs + [-f for f in fs]
+    thresh = Fraction(1, 2 ** 16)
+    for nlo, nhi in ranges:
+        for nq in range(nlo - 4, nhi + 5):
+            nc = _clamp(nq, nlo, nhi)
+            for f in fs:
+                x = -nq + f                      # w' rcp, with nq = -rint(x) the fast decision
+                g = x + nc
+                fires = abs(g * g - Fraction(1, 4)) <= thresh
+                if abs(f) >= Fraction(1, 2) - eps:
+                    # the IEEE rounding may take the neighbour on f's side
+                    nq_other = nq - 1 if f > 0 else nq + 1
+                    if _clamp(nq_other, nlo, nhi) != nc:
+                        assert fires, (nlo, nhi, nq, f)
+                if nq >= nhi + 2 or nq <= nlo - 2:
+                    assert not fires, (nlo, nhi, nq, f)
