@@ -18,6 +18,7 @@ torch = pytest.importorskip("torch")
 
 from oracle import awq_ref as ref  # noqa: E402
 from post_weight_quantization_stats_b300 import awq, build, synth  # noqa: E402
+from tests.clip_bound import criterion_bound as _criterion_bound  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,22 +37,6 @@ def dev(a):
 
 def host(t):
     return t.cpu().numpy()
-
-
-def _criterion_bound(W16, s, ratios, G, sym, bits, h):
-    """[n_ratio, N, K/G] bound on |e_gpu - e_exact| (see the module docstring)."""
-    W = W16.astype(np.float64)
-    N, K = W.shape
-    out = np.zeros((len(ratios), N, K // G))
-    for j, c in enumerate(ratios):
-        qd = ref.quantize_pack(W16, s, G, sym, bits, clip=np.full((N, K // G), c, np.float32))
-        w_hat = ref.dequantize(qd["qweight"], qd["scales"], qd["zeros"], G, s=s)
-        d = np.abs(W - w_hat)
-        delta = 2.0 ** -22 * (np.abs(W) + np.abs(w_hat))
-        e = (h[None, :] * d * d).reshape(N, K // G, G).sum(axis=2)
-        out[j] = (h[None, :] * (2 * d * delta + delta * delta)).reshape(N, K // G, G).sum(axis=2) \
-            + G * 2.0 ** -24 * e
-    return out
 
 
 def _check_clip(W16, X16, s, G, sym, bits, rows=None):
